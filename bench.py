@@ -1,0 +1,367 @@
+"""Benchmark of the fused hidden-state KL loss (fwd + bwd) on GB300.
+
+One step = hylo_kl_forward + hylo_kl_backward over one synthetic batch of the workload
+(default: the 64K-token Stage-II shape, N=65536, d_s=2048, d_t=4096, V=128256, tau=1,
+token_chunk=4096). Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica of the workload on its own GPU (the
+loss needs no exchange on one GPU; weak scaling). `--impl reference` times the fp64 CPU
+oracle on the host cores on a bounded token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from hybrid_upcycling_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "fused KL fwd+bwd tokens/s and TFLOP/s as % of GB300 dense bf16 peak"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "hybrid_upcycling_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the fused forward kernel from the committed ncu summary, if it
+    was taken from the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "fused_fwd_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_hash") != kernel_source_hash() or kv.get("workload") != workload:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id(local: int) -> str:
+    """nvidia-smi identifier of this process's GPU (its UUID when torch exposes it)."""
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(local)
+
+
+def make_buffers(w, x, dev):
+    from hybrid_upcycling_gb300 import _lib
+    f = dict(dtype=torch.float32, device=dev)
+    b = {
+        "ws": torch.empty(_lib.hylo_kl_workspace_bytes(w.N, w.d_s, w.d_t, w.V, w.token_chunk), dtype=torch.uint8,
+                          device=dev),
+        "kl": torch.empty(w.N, **f), "lse_s": torch.empty(w.N, **f), "lse_t": torch.empty(w.N, **f),
+        "loss": torch.empty(1, **f), "dh": torch.empty(w.N, w.d_s, **f), "dW": torch.empty(w.V, w.d_s, **f),
+    }
+    return b
+
+
+def step(w, x, b, stream, ev=None):
+    from hybrid_upcycling_gb300 import _lib
+    if ev is not None:
+        ev[0].record(stream)
+    _lib.hylo_kl_forward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, w.token_chunk, b["kl"], b["lse_s"],
+                         b["lse_t"], b["loss"], b["ws"], stream=stream)
+    if ev is not None:
+        ev[1].record(stream)
+    _lib.hylo_kl_backward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, w.token_chunk, b["lse_s"], b["lse_t"], 1.0,
+                          b["dh"], b["dW"], b["ws"], stream=stream)
+    if ev is not None:
+        ev[2].record(stream)
+
+
+def launches_per_step(w) -> int:
+    chunks = math.ceil(w.N / min(w.token_chunk, w.N))
+    return 3 + 3 * chunks  # fused fwd + combine + mean; per chunk: fused G + dh GEMM + dW GEMM
+
+
+def cpu_oracle_rate(w, x, sample_tokens: int, repeats: int = 1):
+    """Times the fp64 oracle (forward + backward, as it stands) on `sample_tokens` tokens of the
+    workload with the full vocabulary and hidden sizes; returns tokens/s."""
+    from oracle import kl_oracle as orc
+    rows = torch.arange(sample_tokens) * max(1, w.N // sample_tokens)
+    hs = x["h_s"][rows.to(x["h_s"].device)].double().cpu().numpy()
+    ht = x["h_t"][rows.to(x["h_t"].device)].double().cpu().numpy()
+    Ws = x["W_s"].double().cpu().numpy()
+    Wt = x["W_t"].double().cpu().numpy()
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        orc.kl_forward(hs, Ws, ht, Wt, w.tau, w.token_chunk)
+        orc.kl_backward(hs, Ws, ht, Wt, w.tau, w.token_chunk)
+    dt = time.perf_counter() - t0
+    return sample_tokens * repeats / dt, dt
+
+
+def run_reference(args, w, rank, world):
+    """Reference arm: the fp64 CPU oracle on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    torch.manual_seed(0)
+    x = syn.make_inputs(w, device="cuda" if torch.cuda.is_available() else "cpu")
+    tokens = args.ref_tokens
+    for _ in range(args.warmup):
+        cpu_oracle_rate(w, x, tokens)
+    times = []
+    for _ in range(args.steps):
+        _, dt = cpu_oracle_rate(w, x, tokens)
+        times.append(dt)
+    tot = sum(times)
+    value = tokens * args.steps / tot
+    cores = len(os.sched_getaffinity(0))
+    sample = f"{tokens} tokens of {w.name} per step (full V={w.V}, d_s={w.d_s}, d_t={w.d_t}), fp64 numpy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w):
+    in_bytes = 2 * (w.N * (w.d_s + w.d_t) + w.V * (w.d_s + w.d_t))
+    return {"workload": w.name, "N": w.N, "d_s": w.d_s, "d_t": w.d_t, "V": w.V, "tau": w.tau,
+            "token_chunk": w.token_chunk,
+            "l2": f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB of bf16 inputs per step; no flush)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="stage2_64k", choices=list(syn.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=48, help="oracle tokens per reference-arm step")
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+    w = syn.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from hybrid_upcycling_gb300 import _lib, build
+    if rank == 0:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    _lib.load()
+
+    x = syn.make_inputs(w, device=dev)
+    b = make_buffers(w, x, dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step(w, x, b, stream)
+    _lib.hylo_kl_sync_status(stream)
+
+    # ----------------------------------------------------------------- device-resident timing
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id(local)) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                step(w, x, b, stream, evs[i])
+        torch.cuda.synchronize()
+    barrier()
+    _lib.hylo_kl_sync_status(stream)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_ms = evs[0][0].elapsed_time(evs[-1][2])
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens_per_s = w.N * world * args.steps / (total_ms / 1e3)
+    tflops = w.flops_exec() * world * args.steps / (total_ms / 1e3) / 1e12
+    loss_val = float(b["loss"].item())
+
+    peaks, peak_src = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    fwd_avg = float(np.mean(fwd_ms))
+    fwd_tflops = w.flops_fwd() / (fwd_avg / 1e3) / 1e12
+    traffic = recorded_traffic(w.name)
+
+    # ----------------------------------------------------------------- end-to-end via host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in x.items()}
+        for k in x:
+            host[k].copy_(x[k])
+        xd = {k: torch.empty_like(v) for k, v in x.items()}
+        out_host = {k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True) for k in ("kl", "loss", "dh", "dW")}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+        e2e_steps = max(2, min(args.steps, 5))
+        with torch.cuda.stream(stream):
+            for k in x:  # warm the copy path once
+                xd[k].copy_(host[k], non_blocking=True)
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(e2e_steps):
+                for k in x:
+                    xd[k].copy_(host[k], non_blocking=True)
+                step(w, xd, b, stream)
+                for k in out_host:
+                    out_host[k].copy_(b[k], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": w.N * world * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "api": "hylo_kl_forward + hylo_kl_backward (C ABI) with pinned-host inputs/outputs"}
+        del xd, host, out_host
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, dt = cpu_oracle_rate(w, x, args.cpu_tokens)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"{args.cpu_tokens} tokens of {w.name} (full V and d), fp64 numpy forward+backward, "
+                         f"{dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w),
+            "tflops": tflops, "tflops_unit": "TFLOP/s (4 N V (2 d_s + d_t) executed flops per step)",
+            "pct_of_peak": 100.0 * tflops / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+            "peak_source": peak_src, "fwd_ms": fwd_avg, "bwd_ms": float(np.mean(bwd_ms)), "loss": loss_val,
+            "roofline": {"kernel": "fused_kl_kernel<fwd> (+combine, mean)", "bound": "tensor",
+                         "achieved": fwd_tflops, "peak": peak_sus, "unit": "TFLOP/s", "frac": fwd_tflops / peak_sus,
+                         "traffic": traffic, "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                         "flops_per_launch": w.flops_fwd()},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step(w) * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,61 @@
+// Internal launch interface between the C-ABI host code and the sm_103a kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "sm103_ptx.cuh"
+
+namespace hylo {
+
+// Tile sizes shared by host and device code.
+constexpr int kBM = 128;      // token rows per tile (UMMA M, one TMEM lane per row)
+constexpr int kBK = 64;       // k elements per pipeline stage (one 128-byte swizzle row)
+constexpr int kFusedBN = 256; // vocab columns per fused tile
+constexpr int kGemmBN = 256;  // output columns per gradient-GEMM tile
+constexpr int kMaxSegments = 32;
+constexpr int kStatFields = 6; // teacher max, teacher sum, student max, student sum, A, C
+
+// Parameters of the fused dual-GEMM kernel (forward statistics or backward G tiles).
+struct FusedParams {
+  int N;            // token rows covered by the tensor maps of this launch
+  int V;            // vocabulary size
+  int kb_s, kb_t;   // 64-wide k-blocks of the student / teacher projections
+  int token_tiles;  // ceil(N / 128)
+  int vtiles;       // ceil(V / BN)
+  int nseg;         // vocabulary segments per token tile
+  int units;        // token_tiles * nseg
+  float c;          // log2(e) / tau
+  float inv_tau;    // 1 / tau
+  float* part;      // forward: partial statistics [kStatFields][nseg][N]
+  const float* lse_s;  // backward: per-token log-sum-exps (natural log of sum exp(z/tau))
+  const float* lse_t;
+  float gscale;     // backward: grad_scale / (tau * N_total)
+  WaitCtl ctl;
+};
+
+// Parameters of the dense gradient GEMM C[M, Nc] (=|+=) sum_k A[m, k] B[n, k].
+struct GemmParams {
+  int M, Nc, K;
+  int m_tiles, n_tiles, kblocks, tiles;
+  int accumulate;   // 0: overwrite C, 1: add into C (TMA reduce-add)
+  WaitCtl ctl;
+};
+
+int fused_smem_bytes(bool backward);
+cudaError_t fused_prepare(bool backward);
+cudaError_t launch_fused(bool backward, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
+                         const CUtensorMap& Wt, const CUtensorMap& G, const FusedParams& p, int grid,
+                         cudaStream_t stream);
+cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, float* kl, float* lse_s,
+                           float* lse_t, cudaStream_t stream);
+cudaError_t launch_mean(const float* kl, int N, float* loss, cudaStream_t stream);
+
+// A and B are K-major (false) or MN-major (true).
+int gemm_smem_bytes();
+cudaError_t gemm_prepare(bool a_mn, bool b_mn);
+cudaError_t launch_gemm(bool a_mn, bool b_mn, const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& C,
+                        const GemmParams& p, int grid, cudaStream_t stream);
+
+}  // namespace hylo

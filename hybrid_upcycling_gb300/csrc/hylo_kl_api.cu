@@ -1,0 +1,349 @@
+// Host side of the C ABI declared in include/hylo_kl.h: argument checks, the sm_103 guard,
+// TMA tensor-map construction, the vocabulary-segment heuristic, the backward token-chunk
+// loop, and the per-device status word that kernels use to report a timed-out wait.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/hylo_kl.h"
+#include "hylo_internal.h"
+
+namespace hylo {
+namespace {
+
+__device__ int g_device_status;  // 0, or the first device-side error code since the last read
+
+thread_local std::string g_last_error;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool init = false;
+  bool sm103 = false;
+  int sms = 0;
+  int* status = nullptr;
+  std::string why;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+hylo_status fail(hylo_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+hylo_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(HYLO_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+unsigned long long wait_limit_ns() {
+  static const unsigned long long v = [] {
+    const char* s = std::getenv("HYLO_KL_WAIT_LIMIT_MS");
+    long long ms = s ? std::atoll(s) : 5000;
+    if (ms <= 0) ms = 5000;
+    return static_cast<unsigned long long>(ms) * 1000000ull;
+  }();
+  return v;
+}
+
+// Looks up (once per device) the architecture, SM count, status-word address and kernel
+// attributes of the current device.
+hylo_status current_device(DeviceState** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(HYLO_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.sm103 = (major == 10 && minor == 3);
+    if (!d.sm103) {
+      char b[128];
+      snprintf(b, sizeof(b), "device %d is sm_%d%d; this library runs only on sm_103 (GB300)", dev, major, minor);
+      d.why = b;
+    } else {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+      d.status = static_cast<int*>(p);
+      if ((e = fused_prepare(false)) != cudaSuccess || (e = fused_prepare(true)) != cudaSuccess ||
+          (e = gemm_prepare(false, true)) != cudaSuccess || (e = gemm_prepare(true, true)) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute");
+      if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+          return fail(HYLO_ERR_CUDA, "cannot resolve cuTensorMapEncodeTiled from the driver");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      }
+    }
+    d.init = true;
+  }
+  if (!d.sm103) return fail(HYLO_ERR_ARCH, "%s", d.why.c_str());
+  *out = &d;
+  return HYLO_OK;
+}
+
+// 2-D tensor map, 128-byte swizzle, zero fill outside the tensor.
+hylo_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(HYLO_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult %d", static_cast<int>(r));
+  return HYLO_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t chunk_rows(int64_t N, int64_t token_chunk) {
+  int64_t c = token_chunk <= 0 ? 4096 : token_chunk;
+  return c < N ? c : N;
+}
+
+bool sizes_ok(int64_t N, int64_t d_s, int64_t d_t, int64_t V) {
+  return N >= 1 && V >= 1 && N <= 0x7fffffffLL && V <= 0x7fffffffLL && d_s >= 8 && d_t >= 8 && d_s <= 65536 &&
+         d_t <= 65536 && d_s % 8 == 0 && d_t % 8 == 0;
+}
+
+size_t fwd_bytes(int64_t N) { return static_cast<size_t>(kStatFields) * kMaxSegments * N * sizeof(float); }
+
+size_t bwd_bytes(int64_t N, int64_t V, int64_t token_chunk) {
+  const int64_t vpad = cdiv(V, 8) * 8;
+  return static_cast<size_t>(chunk_rows(N, token_chunk)) * vpad * 2;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Number of vocabulary segments per token tile: the work units (token tile, segment) are dealt
+// round-robin to one persistent CTA per SM, so pick the split that minimises
+// waves x (vocab tiles per segment), with a small cost per extra segment.
+int choose_segments(int64_t token_tiles, int64_t vtiles, int sms) {
+  int best = 1;
+  double best_cost = 1e300;
+  for (int s = 1; s <= kMaxSegments && s <= vtiles; ++s) {
+    const int64_t units = token_tiles * s;
+    const int64_t waves = cdiv(units, sms);
+    const int64_t per = cdiv(vtiles, s);
+    const double cost = static_cast<double>(waves * per) * (1.0 + 0.002 * s);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+hylo_status check_common(const void* h_s, const void* W_s, const void* h_t, const void* W_t, int64_t N, int64_t d_s,
+                         int64_t d_t, int64_t V, float tau, void* workspace, size_t workspace_bytes,
+                         size_t need) {
+  if (!h_s || !W_s || !h_t || !W_t || !workspace) return fail(HYLO_ERR_NULL, "a required pointer is NULL");
+  if (!sizes_ok(N, d_s, d_t, V))
+    return fail(HYLO_ERR_DIM, "invalid sizes N=%lld d_s=%lld d_t=%lld V=%lld (d must be a multiple of 8, 8..65536)",
+                static_cast<long long>(N), static_cast<long long>(d_s), static_cast<long long>(d_t),
+                static_cast<long long>(V));
+  if (!aligned(h_s, 16) || !aligned(W_s, 16) || !aligned(h_t, 16) || !aligned(W_t, 16))
+    return fail(HYLO_ERR_ALIGN, "input pointers must be 16-byte aligned");
+  if (!aligned(workspace, 256)) return fail(HYLO_ERR_ALIGN, "workspace must be 256-byte aligned");
+  if (!(std::isfinite(tau) && tau > 0.f)) return fail(HYLO_ERR_TAU, "tau must be finite and > 0");
+  if (workspace_bytes < need)
+    return fail(HYLO_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu required", workspace_bytes, need);
+  return HYLO_OK;
+}
+
+}  // namespace
+}  // namespace hylo
+
+using namespace hylo;
+
+extern "C" {
+
+size_t hylo_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V, int64_t token_chunk) {
+  g_last_error.clear();
+  if (!sizes_ok(N, d_s, d_t, V)) return 0;
+  const size_t f = round256(fwd_bytes(N)), b = round256(bwd_bytes(N, V, token_chunk));
+  return f > b ? f : b;
+}
+
+hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t, const uint16_t* W_t,
+                            int64_t N, int64_t d_s, int64_t d_t, int64_t V, float tau, int64_t token_chunk,
+                            float* kl, float* lse_s, float* lse_t, float* loss, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
+  g_last_error.clear();
+  (void)token_chunk;  // the forward needs O(N) scratch whatever the chunk
+  if (!kl || !lse_s || !lse_t || !loss) return fail(HYLO_ERR_NULL, "an output pointer is NULL");
+  hylo_status st = check_common(h_s, W_s, h_t, W_t, N, d_s, d_t, V, tau, workspace, workspace_bytes,
+                                sizes_ok(N, d_s, d_t, V) ? fwd_bytes(N) : 0);
+  if (st != HYLO_OK) return st;
+  DeviceState* dev = nullptr;
+  if ((st = current_device(&dev)) != HYLO_OK) return st;
+
+  CUtensorMap m_hs, m_Ws, m_ht, m_Wt;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if ((st = make_map(&m_hs, h_s, bf, d_s, N, d_s * 2, kBK, kBM)) != HYLO_OK) return st;
+  if ((st = make_map(&m_ht, h_t, bf, d_t, N, d_t * 2, kBK, kBM)) != HYLO_OK) return st;
+  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, kFusedBN)) != HYLO_OK) return st;
+  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, kFusedBN)) != HYLO_OK) return st;
+
+  FusedParams p{};
+  p.N = static_cast<int>(N);
+  p.V = static_cast<int>(V);
+  p.kb_s = static_cast<int>(cdiv(d_s, kBK));
+  p.kb_t = static_cast<int>(cdiv(d_t, kBK));
+  p.token_tiles = static_cast<int>(cdiv(N, kBM));
+  p.vtiles = static_cast<int>(cdiv(V, kFusedBN));
+  p.nseg = choose_segments(p.token_tiles, p.vtiles, dev->sms);
+  p.units = p.token_tiles * p.nseg;
+  p.c = 1.4426950408889634f / tau;
+  p.inv_tau = 1.0f / tau;
+  p.part = static_cast<float*>(workspace);
+  p.ctl = WaitCtl{dev->status, wait_limit_ns()};
+  const int grid = p.units < dev->sms ? p.units : dev->sms;
+
+  cudaError_t e = launch_fused(false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
+  e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launch combine");
+  e = launch_mean(kl, p.N, loss, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launch mean");
+  return HYLO_OK;
+}
+
+hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t, const uint16_t* W_t,
+                             int64_t N, int64_t d_s, int64_t d_t, int64_t V, float tau, int64_t token_chunk,
+                             const float* lse_s, const float* lse_t, float grad_scale, float* dh_s, float* dW_s,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  g_last_error.clear();
+  if (!lse_s || !lse_t || !dh_s || !dW_s) return fail(HYLO_ERR_NULL, "an lse or gradient pointer is NULL");
+  hylo_status st = check_common(h_s, W_s, h_t, W_t, N, d_s, d_t, V, tau, workspace, workspace_bytes,
+                                sizes_ok(N, d_s, d_t, V) ? bwd_bytes(N, V, token_chunk) : 0);
+  if (st != HYLO_OK) return st;
+  if (!std::isfinite(grad_scale)) return fail(HYLO_ERR_TAU, "grad_scale must be finite");
+  if (!aligned(dh_s, 16) || !aligned(dW_s, 16)) return fail(HYLO_ERR_ALIGN, "gradient pointers must be 16-byte aligned");
+  DeviceState* dev = nullptr;
+  if ((st = current_device(&dev)) != HYLO_OK) return st;
+
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const int64_t chunk = chunk_rows(N, token_chunk);
+  const int64_t vpad = cdiv(V, 8) * 8;
+  uint16_t* G = static_cast<uint16_t*>(workspace);
+
+  CUtensorMap m_Ws, m_Wt, m_WsB, m_dW;
+  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, kFusedBN)) != HYLO_OK) return st;
+  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, kFusedBN)) != HYLO_OK) return st;
+  if ((st = make_map(&m_WsB, W_s, bf, d_s, V, d_s * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major B of dh
+  if ((st = make_map(&m_dW, dW_s, f32, d_s, V, d_s * 4, 32, 32)) != HYLO_OK) return st;
+
+  const WaitCtl ctl{dev->status, wait_limit_ns()};
+  const float gscale = static_cast<float>(static_cast<double>(grad_scale) / (static_cast<double>(tau) * N));
+
+  for (int64_t c0 = 0; c0 < N; c0 += chunk) {
+    const int64_t R = (N - c0) < chunk ? (N - c0) : chunk;
+    const uint16_t* hs_c = h_s + c0 * d_s;
+    const uint16_t* ht_c = h_t + c0 * d_t;
+    CUtensorMap m_hs, m_ht, m_Gst, m_GA, m_GT, m_hsB, m_dh;
+    if ((st = make_map(&m_hs, hs_c, bf, d_s, R, d_s * 2, kBK, kBM)) != HYLO_OK) return st;
+    if ((st = make_map(&m_ht, ht_c, bf, d_t, R, d_t * 2, kBK, kBM)) != HYLO_OK) return st;
+    if ((st = make_map(&m_Gst, G, bf, V, R, vpad * 2, 64, 32)) != HYLO_OK) return st;       // G tile stores
+    if ((st = make_map(&m_GA, G, bf, V, R, vpad * 2, kBK, kBM)) != HYLO_OK) return st;      // K-major A of dh
+    if ((st = make_map(&m_GT, G, bf, V, R, vpad * 2, 64, kBK)) != HYLO_OK) return st;       // MN-major A of dW
+    if ((st = make_map(&m_hsB, hs_c, bf, d_s, R, d_s * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major B of dW
+    if ((st = make_map(&m_dh, dh_s + c0 * d_s, f32, d_s, R, d_s * 4, 32, 32)) != HYLO_OK) return st;
+
+    FusedParams p{};
+    p.N = static_cast<int>(R);
+    p.V = static_cast<int>(V);
+    p.kb_s = static_cast<int>(cdiv(d_s, kBK));
+    p.kb_t = static_cast<int>(cdiv(d_t, kBK));
+    p.token_tiles = static_cast<int>(cdiv(R, kBM));
+    p.vtiles = static_cast<int>(cdiv(V, kFusedBN));
+    p.nseg = choose_segments(p.token_tiles, p.vtiles, dev->sms);
+    p.units = p.token_tiles * p.nseg;
+    p.c = 1.4426950408889634f / tau;
+    p.inv_tau = 1.0f / tau;
+    p.lse_s = lse_s + c0;
+    p.lse_t = lse_t + c0;
+    p.gscale = gscale;
+    p.ctl = ctl;
+    int grid = p.units < dev->sms ? p.units : dev->sms;
+    cudaError_t e = launch_fused(true, m_hs, m_Ws, m_ht, m_Wt, m_Gst, p, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launch fused backward");
+
+    GemmParams gh{};
+    gh.M = static_cast<int>(R);
+    gh.Nc = static_cast<int>(d_s);
+    gh.K = static_cast<int>(V);
+    gh.m_tiles = static_cast<int>(cdiv(R, kBM));
+    gh.n_tiles = static_cast<int>(cdiv(d_s, kGemmBN));
+    gh.kblocks = static_cast<int>(cdiv(V, kBK));
+    gh.tiles = gh.m_tiles * gh.n_tiles;
+    gh.accumulate = 0;
+    gh.ctl = ctl;
+    grid = gh.tiles < dev->sms ? gh.tiles : dev->sms;
+    e = launch_gemm(false, true, m_GA, m_WsB, m_dh, gh, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launch dh GEMM");
+
+    GemmParams gw{};
+    gw.M = static_cast<int>(V);
+    gw.Nc = static_cast<int>(d_s);
+    gw.K = static_cast<int>(R);
+    gw.m_tiles = static_cast<int>(cdiv(V, kBM));
+    gw.n_tiles = static_cast<int>(cdiv(d_s, kGemmBN));
+    gw.kblocks = static_cast<int>(cdiv(R, kBK));
+    gw.tiles = gw.m_tiles * gw.n_tiles;
+    gw.accumulate = c0 > 0 ? 1 : 0;
+    gw.ctl = ctl;
+    grid = gw.tiles < dev->sms ? gw.tiles : dev->sms;
+    e = launch_gemm(true, true, m_GT, m_hsB, m_dW, gw, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launch dW GEMM");
+  }
+  return HYLO_OK;
+}
+
+hylo_status hylo_kl_sync_status(cudaStream_t stream) {
+  g_last_error.clear();
+  DeviceState* dev = nullptr;
+  hylo_status st = current_device(&dev);
+  if (st != HYLO_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int code = 0;
+  if ((e = cudaMemcpyFromSymbol(&code, g_device_status, sizeof(int))) != cudaSuccess)
+    return cuda_fail(e, "read device status");
+  if (code != 0) {
+    const int zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int))) != cudaSuccess)
+      return cuda_fail(e, "clear device status");
+    return fail(HYLO_ERR_TIMEOUT, "a device-side pipeline wait timed out (site %d)", code - kDevTimeoutBase);
+  }
+  return HYLO_OK;
+}
+
+const char* hylo_kl_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+/*
+ * hylo_kl.h — C ABI of the fused hidden-state KL distillation loss (GB300, sm_103a).
+ *
+ * The operation. Stage II of HyLo trains the upcycled hybrid student end to end against a
+ * Llama-3.1-8B teacher with a KL loss between the two next-token distributions, weight 1.0
+ * and no cross-entropy term (HyLo-Llama-8MLA8GDN-8K-SFT reading notes, kwkr.cn, section
+ * "two-stage training recipe", Stage II). To fit an 8B teacher at 64K tokens the loss takes
+ * the FINAL HIDDEN STATES of both models (the teacher's LM head is skipped), applies both
+ * LM-head projections itself, fuses the softmax with the KL, and walks the tokens in chunks
+ * of 4096 (Long-Context Aware Upcycling digest, ftxj.github.io, section Method; section Key
+ * Ideas). The pages print no formula; this library computes, for every token n:
+ *
+ *     z_s = h_s[n] W_s^T,  z_t = h_t[n] W_t^T                 (over the full vocabulary V)
+ *     p_x = softmax(z_x / tau),  lse_x[n] = logsumexp(z_x / tau)
+ *     kl[n] = KL(p_t || p_s) = sum_v p_t,v (log p_t,v - log p_s,v)
+ *     loss  = (1/N) sum_n kl[n]
+ * and the gradients of grad_scale * loss with respect to the student's h_s and W_s:
+ *     G[n, v] = grad_scale * (p_s,v - p_t,v) / (tau N),  dh_s = G W_s,  dW_s = G^T h_s.
+ * The N x V logit tensor is never stored. No teacher gradients (the teacher is frozen).
+ *
+ * Conventions shared by every call:
+ *   - All pointers except `stream` and `workspace` sizes are DEVICE pointers on the current
+ *     CUDA device, owned by the caller; the library never allocates or frees memory.
+ *   - h_s [N, d_s], h_t [N, d_t], W_s [V, d_s], W_t [V, d_t]: bfloat16 bit patterns
+ *     (uint16), row-major and contiguous (W like nn.Linear.weight: [vocab, hidden]).
+ *   - d_s and d_t must be multiples of 8 (16-byte rows); every pointer must be 16-byte
+ *     aligned. 1 <= N, V <= 2^31 - 1; 8 <= d_s, d_t <= 65536; tau finite and > 0.
+ *   - float outputs are fp32. Every call is asynchronous on `stream` (a cudaStream_t;
+ *     NULL = the legacy default stream) and returns after enqueueing its kernels.
+ *   - The returned status covers argument checks, the architecture check and launch errors.
+ *     Device-side failures (a pipeline wait that exceeded its time limit) are recorded in a
+ *     per-device status word; read it with hylo_kl_sync_status().
+ *   - `workspace` is device scratch of at least hylo_kl_workspace_bytes(...) bytes, 256-byte
+ *     aligned, not shared with a call still running on another stream.
+ *   - Calls require an sm_103 device (GB300); otherwise HYLO_ERR_ARCH. There is no fallback.
+ */
+#ifndef HYLO_KL_H
+#define HYLO_KL_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HYLO_OK = 0,
+  HYLO_ERR_NULL = -1,      /* a required pointer is NULL */
+  HYLO_ERR_DIM = -2,       /* a size is out of range or not a multiple of 8 where required */
+  HYLO_ERR_ALIGN = -3,     /* a pointer is not 16-byte aligned (workspace: 256-byte) */
+  HYLO_ERR_TAU = -4,       /* tau is not finite and > 0, or grad_scale is not finite */
+  HYLO_ERR_WORKSPACE = -5, /* workspace_bytes is smaller than hylo_kl_workspace_bytes() */
+  HYLO_ERR_CUDA = -6,      /* a CUDA runtime or driver call failed (see hylo_kl_last_error) */
+  HYLO_ERR_TIMEOUT = -7,   /* a device-side pipeline wait exceeded its limit (device status) */
+  HYLO_ERR_ARCH = -8       /* the current device is not sm_103 */
+} hylo_status;
+
+/* Bytes of device workspace that hylo_kl_forward and hylo_kl_backward need for these sizes.
+ * It is O(N) for the forward (per-token partial softmax statistics) and
+ * O(token_chunk * V) bf16 for the backward (the gradient of one token chunk's logits),
+ * never O(N * V). Returns 0 for invalid sizes. token_chunk <= 0 means 4096. */
+size_t hylo_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
+                               int64_t token_chunk);
+
+/* Forward: kl[N], lse_s[N], lse_t[N] (natural-log units of z/tau) and loss[0] = mean(kl).
+ * One fused pass: each CTA computes student and teacher logit tiles on the tensor cores and
+ * folds them into running softmax/KL statistics; nothing of size N x V is written.
+ * token_chunk (<= 0 means 4096) does not change the results; the forward uses O(N) scratch
+ * whatever its value. kl, lse_s, lse_t and loss may not alias the inputs. */
+hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s,
+                            const uint16_t* h_t, const uint16_t* W_t,
+                            int64_t N, int64_t d_s, int64_t d_t, int64_t V,
+                            float tau, int64_t token_chunk,
+                            float* kl, float* lse_s, float* lse_t, float* loss,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Backward: dh_s [N, d_s] and dW_s [V, d_s] (fp32, OVERWRITTEN, not accumulated) for
+ * grad_scale * loss, from the lse_s / lse_t that hylo_kl_forward wrote for the same inputs.
+ * Per token chunk it recomputes both logit tiles, forms G in bf16 in the workspace
+ * (token_chunk x V), then runs dh_s = G W_s and dW_s += G^T h_s on the tensor cores.
+ * Results match for any token_chunk up to fp32 summation order. */
+hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s,
+                             const uint16_t* h_t, const uint16_t* W_t,
+                             int64_t N, int64_t d_s, int64_t d_t, int64_t V,
+                             float tau, int64_t token_chunk,
+                             const float* lse_s, const float* lse_t, float grad_scale,
+                             float* dh_s, float* dW_s,
+                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, then returns and clears the current device's status word:
+ * HYLO_OK, or HYLO_ERR_TIMEOUT if a kernel gave up on a pipeline wait since the last read
+ * (its outputs are then invalid), or HYLO_ERR_CUDA if the synchronisation failed. */
+hylo_status hylo_kl_sync_status(cudaStream_t stream);
+
+/* Thread-local text describing the last non-OK status returned on this thread ("" if none).
+ * The pointer stays valid until the next library call on the same thread. */
+const char* hylo_kl_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYLO_KL_H */

@@ -1,0 +1,103 @@
+"""Host-side checks of the C ABI: the shared library builds and loads, exports every entry
+point include/hylo_kl.h declares, sizes its workspace as documented, and rejects bad
+arguments before touching the GPU (these calls never launch a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from hybrid_upcycling_gb300 import build, _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(hylo_\w+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_symbols()
+    assert {"hylo_kl_forward", "hylo_kl_backward", "hylo_kl_workspace_bytes"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(_lib.EXPORTS) <= names
+
+
+def test_workspace_bytes(lib):
+    N, d_s, d_t, V = 65536, 2048, 4096, 128256
+    fwd = 6 * 32 * N * 4
+    bwd = 4096 * V * 2
+    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096) == max(fwd, bwd)
+    # O(N + token_chunk * V), never N * V
+    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 1024) == max(fwd, 1024 * V * 2)
+    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096) < N * V * 2 // 8
+    # chunk larger than N is clamped to N; <= 0 means 4096
+    assert _lib.hylo_kl_workspace_bytes(100, 64, 128, 513, 100000) == max(6 * 32 * 100 * 4, ((100 * 520 * 2 + 255) // 256) * 256)
+    assert _lib.hylo_kl_workspace_bytes(8192, 64, 64, 1000, 0) == _lib.hylo_kl_workspace_bytes(8192, 64, 64, 1000, 4096)
+    # invalid sizes give 0
+    assert _lib.hylo_kl_workspace_bytes(0, 64, 64, 10, 4096) == 0
+    assert _lib.hylo_kl_workspace_bytes(10, 60, 64, 10, 4096) == 0
+    assert _lib.hylo_kl_workspace_bytes(10, 64, 64, 0, 4096) == 0
+
+
+FAKE = 0x10000  # a 256-byte aligned non-null address; never dereferenced by these calls
+
+
+def _fwd(lib, **kw):
+    a = dict(h_s=FAKE, W_s=FAKE, h_t=FAKE, W_t=FAKE, N=16, d_s=64, d_t=128, V=100, tau=1.0, chunk=4096,
+             kl=FAKE, lse_s=FAKE, lse_t=FAKE, loss=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.hylo_kl_forward(a["h_s"], a["W_s"], a["h_t"], a["W_t"], a["N"], a["d_s"], a["d_t"], a["V"],
+                               a["tau"], a["chunk"], a["kl"], a["lse_s"], a["lse_t"], a["loss"], a["ws"],
+                               a["wsb"], a["stream"])
+
+
+def _bwd(lib, **kw):
+    a = dict(h_s=FAKE, W_s=FAKE, h_t=FAKE, W_t=FAKE, N=16, d_s=64, d_t=128, V=100, tau=1.0, chunk=4096,
+             lse_s=FAKE, lse_t=FAKE, gs=1.0, dh=FAKE, dW=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.hylo_kl_backward(a["h_s"], a["W_s"], a["h_t"], a["W_t"], a["N"], a["d_s"], a["d_t"], a["V"],
+                                a["tau"], a["chunk"], a["lse_s"], a["lse_t"], a["gs"], a["dh"], a["dW"], a["ws"],
+                                a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(h_s=None), -1), (dict(W_t=None), -1), (dict(kl=None), -1), (dict(ws=None), -1),
+    (dict(N=0), -2), (dict(V=0), -2), (dict(d_s=60), -2), (dict(d_t=4), -2), (dict(d_s=70000), -2),
+    (dict(h_s=FAKE + 8), -3), (dict(ws=FAKE + 16), -3),
+    (dict(tau=0.0), -4), (dict(tau=-1.0), -4), (dict(tau=float("inf")), -4), (dict(tau=float("nan")), -4),
+    (dict(wsb=16), -5),
+])
+def test_forward_rejects_bad_arguments(lib, kw, status):
+    assert _fwd(lib, **kw) == status
+    assert lib.hylo_kl_last_error()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(lse_s=None), -1), (dict(dW=None), -1), (dict(N=-5), -2), (dict(d_t=12), -2),
+    (dict(W_s=FAKE + 4), -3), (dict(dh=FAKE + 4), -3), (dict(tau=float("nan")), -4),
+    (dict(gs=float("inf")), -4), (dict(wsb=100), -5),
+])
+def test_backward_rejects_bad_arguments(lib, kw, status):
+    assert _bwd(lib, **kw) == status
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
+def test_valid_call_without_gpu_fails_cleanly(lib):
+    st = _fwd(lib)
+    assert st in (-6, -8)
+    assert lib.hylo_kl_last_error()

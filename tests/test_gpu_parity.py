@@ -1,0 +1,246 @@
+"""GPU parity: the sm_103a library (through its C ABI) against the fp64 oracle.
+
+Tolerances (stated for the fused hidden-state KL):
+  per token   |kl_gpu - kl_ref| <= 1e-3 (1 + kl_ref)
+  mean loss   |L_gpu - L_ref| <= 1e-4 |L_ref|
+  gradients   ||g_gpu - g_ref||_F <= 2e-3 ||g_ref||_F   for dh_s and dW_s
+  lse         |lse_gpu - lse_ref| <= 2e-5 (1 + |lse_ref|)   (fp32 logits and sums; derived)
+Small shapes are compared densely; the full workload sizes on sampled tokens (the oracle
+recomputes each sampled token over the whole vocabulary), on a dense full-vocabulary token
+subset, and through invariants that hold at any size.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from hybrid_upcycling_gb300 import _lib, build, synthetic as syn
+from oracle import kl_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+TOL_KL, TOL_LOSS, TOL_GRAD, TOL_LSE = 1e-3, 1e-4, 2e-3, 2e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    return _lib.load()
+
+
+def f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def run(x, tau, token_chunk=4096, grad_scale=1.0, backward=True, stream=None):
+    dev = x["h_s"].device
+    N, d_s = x["h_s"].shape
+    V, d_t = x["W_t"].shape
+    ws = torch.empty(_lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, token_chunk), dtype=torch.uint8, device=dev)
+    kl = torch.full((N,), float("nan"), device=dev)
+    lse_s = torch.full((N,), float("nan"), device=dev)
+    lse_t = torch.full((N,), float("nan"), device=dev)
+    loss = torch.full((1,), float("nan"), device=dev)
+    _lib.hylo_kl_forward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], tau, token_chunk, kl, lse_s, lse_t, loss, ws,
+                         stream=stream)
+    out = dict(kl=kl, lse_s=lse_s, lse_t=lse_t, loss=loss)
+    if backward:
+        dh = torch.full((N, d_s), float("nan"), device=dev)
+        dW = torch.full((V, d_s), float("nan"), device=dev)
+        _lib.hylo_kl_backward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], tau, token_chunk, lse_s, lse_t, grad_scale,
+                              dh, dW, ws, stream=stream)
+        out.update(dh=dh, dW=dW)
+    _lib.hylo_kl_sync_status(stream)
+    return out
+
+
+def frob_rel(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def check_dense(x, tau, token_chunk=4096, grad_scale=1.0, loss_abs=0.0):
+    g = run(x, tau, token_chunk, grad_scale)
+    hs, Ws, ht, Wt = (f64(x[k]) for k in ("h_s", "W_s", "h_t", "W_t"))
+    kl, ls, lt, loss = orc.kl_forward(hs, Ws, ht, Wt, tau)
+    dh, dW = orc.kl_backward(hs, Ws, ht, Wt, tau, grad_scale=grad_scale)
+    gk = f64(g["kl"])
+    assert np.all(np.isfinite(gk))
+    assert np.all(np.abs(gk - kl) <= TOL_KL * (1 + kl)), np.max(np.abs(gk - kl) / (1 + kl))
+    gl = float(g["loss"].item())
+    assert abs(gl - loss) <= TOL_LOSS * abs(loss) + loss_abs, (gl, loss)
+    assert np.all(np.abs(f64(g["lse_s"]) - ls) <= TOL_LSE * (1 + np.abs(ls)))
+    assert np.all(np.abs(f64(g["lse_t"]) - lt) <= TOL_LSE * (1 + np.abs(lt)))
+    assert frob_rel(f64(g["dh"]), dh) <= TOL_GRAD, frob_rel(f64(g["dh"]), dh)
+    assert frob_rel(f64(g["dW"]), dW) <= TOL_GRAD, frob_rel(f64(g["dW"]), dW)
+    return g
+
+
+def gen(N, d_s, d_t, V, seed, w_std=0.05, normalise=False, device="cuda"):
+    w = syn.Workload("case", 0, N, d_s, d_t, V, 1.0, w_std, normalise)
+    return syn.make_inputs(w, device=device, seed=seed)
+
+
+# ------------------------------------------------------------------------- dense, small shapes
+
+@pytest.mark.parametrize("token_chunk", [4096, 7])
+def test_tiny_workload(token_chunk):
+    w = syn.WORKLOADS["tiny"]
+    check_dense(syn.make_inputs(w, device="cuda"), w.tau, token_chunk)
+
+
+def test_rational_golden_case():
+    import importlib.util
+    import json
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    spec = importlib.util.spec_from_file_location("rational_case", os.path.join(here, "rational_case.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    ref = json.load(open(os.path.join(here, "rational_case.json")))
+    x = {k: torch.tensor(v, dtype=torch.float64).to(torch.bfloat16).cuda()
+         for k, v in zip(("h_s", "W_s", "h_t", "W_t"), mod.inputs())}
+    for k, v in zip(("h_s", "W_s", "h_t", "W_t"), mod.inputs()):
+        assert np.array_equal(f64(x[k]), v)  # the rationals are exact in bf16
+    g = run(x, ref["tau"], grad_scale=ref["grad_scale"])
+    kl = np.array(ref["kl"])
+    assert np.all(np.abs(f64(g["kl"]) - kl) <= TOL_KL * (1 + kl))
+    assert abs(g["loss"].item() - ref["loss"]) <= TOL_LOSS * ref["loss"]
+    assert frob_rel(f64(g["dh"]), np.array(ref["dh_s"])) <= TOL_GRAD
+    assert frob_rel(f64(g["dW"]), np.array(ref["dW_s"])) <= TOL_GRAD
+
+
+@pytest.mark.parametrize("N,d_s,d_t,V,tau,chunk,gs", [
+    (300, 136, 200, 1000, 0.7, 128, 1.0),      # ragged everything, 3 chunks
+    (1061, 256, 512, 8269, 2.0, 512, 0.37),    # several tiles each way, ragged tails
+    (129, 64, 64, 257, 1.0, 4096, 1.0),        # one row and one column past a tile
+    (1, 8, 8, 3, 1.0, 4096, 1.0),              # minimum sizes
+])
+def test_ragged_shapes(N, d_s, d_t, V, tau, chunk, gs):
+    x = gen(N, d_s, d_t, V, seed=N + V, w_std=0.1)
+    check_dense(x, tau, chunk, gs, loss_abs=1e-7)
+
+
+def test_vocab_of_one_gives_zero():
+    """V = 1: both distributions are a point mass, KL = 0 and G = 0 up to fp32 rounding of
+    p = exp(z/tau - lse) = 1."""
+    N = 33
+    x = gen(N, 16, 24, 1, seed=5)
+    g = run(x, 1.5)
+    assert torch.all(g["kl"].abs() <= 1e-6)
+    z_s = (x["h_s"].double() @ x["W_s"].double().T)[:, 0]
+    assert torch.allclose(g["lse_s"].double(), z_s / 1.5, rtol=1e-6, atol=1e-6)
+    gmax = 4e-7 / (1.5 * N)  # |p_s - p_t| <= a few ulp of 1
+    assert g["dh"].abs().max().item() <= gmax * x["W_s"].float().abs().max().item() + 1e-30
+    assert g["dW"].abs().max().item() <= gmax * N * x["h_s"].float().abs().max().item() + 1e-30
+
+
+def test_identical_student_and_teacher_give_exact_zero():
+    x = gen(200, 128, 128, 3000, seed=9, w_std=0.1)
+    x["h_t"], x["W_t"] = x["h_s"].clone(), x["W_s"].clone()
+    g = run(x, 1.0, token_chunk=64)
+    assert torch.all(g["kl"] == 0), g["kl"].abs().max()
+    assert torch.all(g["dh"] == 0) and torch.all(g["dW"] == 0)
+    assert torch.equal(g["lse_s"], g["lse_t"])
+
+
+def test_near_converged_cancellation():
+    """Student logits = teacher logits + 1e-2-scale noise: KL ~ 7e-5 from two ~log V terms."""
+    w = syn.WORKLOADS["llama3b_nearconv"].with_sizes(N=700, V=6000)
+    g = check_dense(syn.make_inputs(w, device="cuda"), 1.0, 256)
+    assert 2e-5 < g["loss"].item() < 2e-4
+
+
+def test_token_chunk_invariance_and_determinism():
+    x = gen(600, 128, 256, 5000, seed=3, w_std=0.08)
+    a = run(x, 1.0, token_chunk=4096)
+    b = run(x, 1.0, token_chunk=100)
+    c = run(x, 1.0, token_chunk=4096)
+    for k in ("kl", "lse_s", "lse_t", "loss", "dh", "dW"):
+        assert torch.equal(a[k], c[k]), k  # bit-identical reruns
+    for k in ("kl", "lse_s", "lse_t", "loss", "dh"):
+        assert torch.equal(a[k], b[k]), k  # per-token results do not depend on the chunk
+    assert frob_rel(f64(b["dW"]), f64(a["dW"])) < 1e-6  # dW differs only by fp32 summation order
+
+
+def test_runs_on_a_side_stream():
+    x = gen(256, 64, 128, 700, seed=11)
+    ref = run(x, 1.0)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        got = run(x, 1.0, stream=s)
+    s.synchronize()
+    for k in ref:
+        assert torch.equal(ref[k], got[k]), k
+
+
+def test_autograd_wrapper():
+    from hybrid_upcycling_gb300.kl import fused_hidden_state_kl
+    w = syn.WORKLOADS["tiny"]
+    x = syn.make_inputs(w, device="cuda")
+    h_s = x["h_s"].clone().requires_grad_(True)
+    W_s = x["W_s"].clone().requires_grad_(True)
+    loss, kl = fused_hidden_state_kl(h_s, W_s, x["h_t"], x["W_t"], 1.0)
+    (2.0 * loss).backward()
+    ref = orc.kl_backward(f64(x["h_s"]), f64(x["W_s"]), f64(x["h_t"]), f64(x["W_t"]), 1.0, grad_scale=2.0)
+    # the wrapper returns bf16 gradients (the input dtype): allow bf16 rounding on top
+    assert frob_rel(f64(h_s.grad), ref[0]) <= TOL_GRAD + 4e-3
+    assert frob_rel(f64(W_s.grad), ref[1]) <= TOL_GRAD + 4e-3
+    assert abs(loss.item() - float(np.mean(f64(kl)))) < 1e-6
+
+
+# ------------------------------------------------------------------- full workload sizes
+
+def _sample_rows(N, chunk, k, seed):
+    rng = np.random.default_rng(seed)
+    fixed = {0, N - 1, min(N - 1, 127), min(N - 1, 128)}
+    for c in range(chunk, N, chunk):
+        fixed |= {c - 1, c}
+    rest = rng.choice(N, size=max(0, k - len(fixed)), replace=False)
+    return np.array(sorted(fixed | set(int(r) for r in rest)))
+
+
+@pytest.mark.parametrize("name", ["llama1b_8b_8k", "stage2_64k", "qwen17b_8b", "llama3b_nearconv"])
+def test_full_size_workload(name):
+    w = syn.WORKLOADS[name]
+    x = syn.make_inputs(w, device="cuda")
+    g = run(x, w.tau, w.token_chunk)
+    N = w.N
+    kl_g = g["kl"].double()
+    assert torch.all(torch.isfinite(kl_g)) and torch.all(torch.isfinite(g["dh"])) and torch.all(torch.isfinite(g["dW"]))
+    # the loss is the mean of the per-token values
+    assert abs(g["loss"].item() - kl_g.mean().item()) <= 1e-6 * abs(kl_g.mean().item())
+    # sampled tokens against the oracle, over the whole vocabulary
+    rows = _sample_rows(N, w.token_chunk, 160, seed=w.seed)
+    Ws, Wt = f64(x["W_s"]), f64(x["W_t"])
+    hs_r, ht_r = f64(x["h_s"][rows]), f64(x["h_t"][rows])
+    kl, ls, lt, dh = orc.kl_rows(hs_r, Ws, ht_r, Wt, w.tau, np.arange(len(rows)), n_total=N)
+    gk = f64(g["kl"][rows])
+    assert np.all(np.abs(gk - kl) <= TOL_KL * (1 + kl)), np.max(np.abs(gk - kl))
+    if w.near_converged:
+        # the cancellation-free form keeps each token's relative error far below the mean-loss bound
+        assert np.all(np.abs(gk - kl) <= TOL_LOSS * kl), np.max(np.abs(gk - kl) / kl)
+    assert abs(gk.mean() - kl.mean()) <= TOL_LOSS * kl.mean()
+    assert np.all(np.abs(f64(g["lse_s"][rows]) - ls) <= TOL_LSE * (1 + np.abs(ls)))
+    assert np.all(np.abs(f64(g["lse_t"][rows]) - lt) <= TOL_LSE * (1 + np.abs(lt)))
+    assert frob_rel(f64(g["dh"][rows]), dh) <= TOL_GRAD
+    # invariants of dW_s at full size: zero column sums, and <dW_s, W_s> = <dh_s, h_s>
+    dW = g["dW"].double()
+    col = dW.sum(0).abs()
+    assert torch.all(col <= 1e-3 * dW.abs().sum(0) + 1e-30)
+    a = (dW * x["W_s"].double()).sum().item()
+    b = (g["dh"].double() * x["h_s"].double()).sum().item()
+    bound = (dW.norm() * x["W_s"].double().norm()).item()
+    assert abs(a - b) <= 1e-4 * bound
+    del g, dW
+    torch.cuda.empty_cache()
+    # dense dW_s over the full vocabulary and hidden size on a token subset (lse from the oracle
+    # would be circular here, so the subset is its own problem with its own mean)
+    sub = rows[:96]
+    xs = {k: x[k][sub].contiguous() if k.startswith("h") else x[k] for k in x}
+    gs = run(xs, w.tau, w.token_chunk, grad_scale=0.5)
+    dh_ref, dW_ref = orc.kl_backward(f64(xs["h_s"]), Ws, f64(xs["h_t"]), Wt, w.tau, grad_scale=0.5)
+    assert frob_rel(f64(gs["dW"]), dW_ref) <= TOL_GRAD
+    assert frob_rel(f64(gs["dh"]), dh_ref) <= TOL_GRAD
