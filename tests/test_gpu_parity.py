@@ -225,7 +225,10 @@ def test_full_size_workload(name):
     assert abs(gk.mean() - kl.mean()) <= TOL_LOSS * kl.mean()
     assert np.all(np.abs(f64(g["lse_s"][rows]) - ls) <= TOL_LSE * (1 + np.abs(ls)))
     assert np.all(np.abs(f64(g["lse_t"][rows]) - lt) <= TOL_LSE * (1 + np.abs(lt)))
-    assert frob_rel(f64(g["dh"][rows]), dh) <= TOL_GRAD
+    e_dh = frob_rel(f64(g["dh"][rows]), dh)
+    print(f"{name}: sampled kl max err {np.max(np.abs(gk - kl)):.2e}, mean rel {abs(gk.mean() - kl.mean()) / kl.mean():.2e}, "
+          f"dh rows rel {e_dh:.2e}")
+    assert e_dh <= TOL_GRAD
     # invariants of dW_s at full size: zero column sums, and <dW_s, W_s> = <dh_s, h_s>
     dW = g["dW"].double()
     col = dW.sum(0).abs()
@@ -233,7 +236,11 @@ def test_full_size_workload(name):
     a = (dW * x["W_s"].double()).sum().item()
     b = (g["dh"].double() * x["h_s"].double()).sum().item()
     bound = (dW.norm() * x["W_s"].double().norm()).item()
-    assert abs(a - b) <= 1e-4 * bound
+    # Both sides sum the same bf16-G products; they differ only by fp32 accumulation, longest
+    # in dh_s (K = V, one accumulator update per 16 products): allow (V/16) * 2^-24 of the bound.
+    acc_tol = max(1e-5, (w.V / 16) * 2.0 ** -24)
+    print(f"{name}: trace gap {abs(a - b) / bound:.2e} (tol {acc_tol:.2e})")
+    assert abs(a - b) <= acc_tol * bound
     del g, dW
     torch.cuda.empty_cache()
     # dense dW_s over the full vocabulary and hidden size on a token subset (lse from the oracle
@@ -242,5 +249,7 @@ def test_full_size_workload(name):
     xs = {k: x[k][sub].contiguous() if k.startswith("h") else x[k] for k in x}
     gs = run(xs, w.tau, w.token_chunk, grad_scale=0.5)
     dh_ref, dW_ref = orc.kl_backward(f64(xs["h_s"]), Ws, f64(xs["h_t"]), Wt, w.tau, grad_scale=0.5)
-    assert frob_rel(f64(gs["dW"]), dW_ref) <= TOL_GRAD
-    assert frob_rel(f64(gs["dh"]), dh_ref) <= TOL_GRAD
+    e_w, e_h = frob_rel(f64(gs["dW"]), dW_ref), frob_rel(f64(gs["dh"]), dh_ref)
+    print(f"{name}: token-subset dense dW rel {e_w:.2e}, dh rel {e_h:.2e}")
+    assert e_w <= TOL_GRAD
+    assert e_h <= TOL_GRAD
