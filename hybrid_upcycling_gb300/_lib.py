@@ -28,7 +28,7 @@ STATUS = {
 }
 
 EXPORTS = ("hylo_kl_workspace_bytes", "hylo_kl_forward", "hylo_kl_backward", "hylo_kl_sync_status",
-           "hylo_kl_last_error")
+           "hylo_kl_last_error", "hylo_kl_forward_noalloc")
 
 
 class HyloError(RuntimeError):
@@ -55,6 +55,8 @@ def load() -> ctypes.CDLL:
     L.hylo_kl_forward.restype = ctypes.c_int
     L.hylo_kl_backward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, f32, vp, vp, vp, sz, vp]
     L.hylo_kl_backward.restype = ctypes.c_int
+    L.hylo_kl_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, vp, vp, vp]
+    L.hylo_kl_forward_noalloc.restype = ctypes.c_int
     L.hylo_kl_sync_status.argtypes = [vp]
     L.hylo_kl_sync_status.restype = ctypes.c_int
     L.hylo_kl_last_error.argtypes = []
@@ -111,6 +113,15 @@ def hylo_kl_backward(h_s, W_s, h_t, W_t, tau: float, token_chunk: int, lse_s, ls
                                    int(token_chunk), _ptr(lse_s), _ptr(lse_t), float(grad_scale), _ptr(dh_s),
                                    _ptr(dW_s), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)))
+
+
+def hylo_kl_forward_noalloc(h_s, W_s, h_t, W_t, tau: float, token_chunk: int, kl, lse_s, lse_t, loss,
+                            stream=None) -> None:
+    """hylo_kl_forward without a workspace: the library's built-in scratch is used instead."""
+    N, d_s, d_t, V = _dims(h_s, W_s, h_t, W_t)
+    _check(load().hylo_kl_forward_noalloc(_ptr(h_s), _ptr(W_s), _ptr(h_t), _ptr(W_t), N, d_s, d_t, V, float(tau),
+                                          int(token_chunk), _ptr(kl), _ptr(lse_s), _ptr(lse_t), _ptr(loss),
+                                          _stream(stream)))
 
 
 def hylo_kl_sync_status(stream=None) -> None:

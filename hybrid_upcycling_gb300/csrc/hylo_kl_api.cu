@@ -347,3 +347,99 @@ hylo_status hylo_kl_sync_status(cudaStream_t stream) {
 const char* hylo_kl_last_error(void) { return g_last_error.c_str(); }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------
+// Forward without caller-provided workspace, for callers that cannot allocate device memory.
+// The per-token partial statistics live in a fixed file-scope device array instead.
+namespace hylo {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+constexpr size_t kNoAllocFloats = kNoAllocScratchBytes / sizeof(float);
+// Largest N whose statistics fit with one vocabulary segment: 16 MiB / (6 fields * 4 B).
+constexpr int64_t kNoAllocMaxTokens = static_cast<int64_t>(kNoAllocFloats / kStatFields);
+
+// Every device that loads this library holds this array until the process exits.
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
+
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Looks up, once per device and with that device current, the device address of the array.
+// Host code must not pass g_noalloc_scratch itself to a kernel: on the host that name is only a
+// stand-in for the device symbol.
+hylo_status noalloc_scratch(float** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(HYLO_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return HYLO_OK;
+}
+
+}  // namespace
+}  // namespace hylo
+
+extern "C" hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t,
+                                               const uint16_t* W_t, int64_t N, int64_t d_s, int64_t d_t, int64_t V,
+                                               float tau, int64_t token_chunk, float* kl, float* lse_s,
+                                               float* lse_t, float* loss, cudaStream_t stream) {
+  g_last_error.clear();
+  (void)token_chunk;
+  if (!h_s || !W_s || !h_t || !W_t || !kl || !lse_s || !lse_t || !loss)
+    return fail(HYLO_ERR_NULL, "a required pointer is NULL");
+  if (!sizes_ok(N, d_s, d_t, V))
+    return fail(HYLO_ERR_DIM, "invalid sizes N=%lld d_s=%lld d_t=%lld V=%lld (d must be a multiple of 8, 8..65536)",
+                static_cast<long long>(N), static_cast<long long>(d_s), static_cast<long long>(d_t),
+                static_cast<long long>(V));
+  if (N > kNoAllocMaxTokens)
+    return fail(HYLO_ERR_DIM, "N=%lld exceeds the %lld tokens whose statistics fit the %zu-byte built-in scratch",
+                static_cast<long long>(N), static_cast<long long>(kNoAllocMaxTokens), kNoAllocScratchBytes);
+  if (!aligned(h_s, 16) || !aligned(W_s, 16) || !aligned(h_t, 16) || !aligned(W_t, 16))
+    return fail(HYLO_ERR_ALIGN, "input pointers must be 16-byte aligned");
+  if (!(std::isfinite(tau) && tau > 0.f)) return fail(HYLO_ERR_TAU, "tau must be finite and > 0");
+  DeviceState* dev = nullptr;
+  hylo_status st = current_device(&dev);
+  if (st != HYLO_OK) return st;
+  float* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != HYLO_OK) return st;
+
+  CUtensorMap m_hs, m_Ws, m_ht, m_Wt;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if ((st = make_map(&m_hs, h_s, bf, d_s, N, d_s * 2, kBK, kBM)) != HYLO_OK) return st;
+  if ((st = make_map(&m_ht, h_t, bf, d_t, N, d_t * 2, kBK, kBM)) != HYLO_OK) return st;
+  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, kFusedBN)) != HYLO_OK) return st;
+  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, kFusedBN)) != HYLO_OK) return st;
+
+  FusedParams p{};
+  p.N = static_cast<int>(N);
+  p.V = static_cast<int>(V);
+  p.kb_s = static_cast<int>(cdiv(d_s, kBK));
+  p.kb_t = static_cast<int>(cdiv(d_t, kBK));
+  p.token_tiles = static_cast<int>(cdiv(N, kBM));
+  p.vtiles = static_cast<int>(cdiv(V, kFusedBN));
+  // as many vocabulary segments as the heuristic wants, but no more than the scratch holds
+  const int64_t fit = static_cast<int64_t>(kNoAllocFloats) / (static_cast<int64_t>(kStatFields) * N);
+  const int want = choose_segments(p.token_tiles, p.vtiles, dev->sms);
+  p.nseg = static_cast<int>(want < fit ? want : fit);
+  p.units = p.token_tiles * p.nseg;
+  p.c = 1.4426950408889634f / tau;
+  p.inv_tau = 1.0f / tau;
+  p.part = scratch;  // every (segment, token) slot read by the combine step is written first
+  p.ctl = WaitCtl{dev->status, wait_limit_ns()};
+  const int grid = p.units < dev->sms ? p.units : dev->sms;
+
+  cudaError_t e = launch_fused(false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
+  e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launch combine");
+  e = launch_mean(kl, p.N, loss, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launch mean");
+  return HYLO_OK;
+}

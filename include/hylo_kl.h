@@ -89,6 +89,28 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s,
                              float* dh_s, float* dW_s,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Forward that allocates nothing and takes no workspace. (The pages describe no such call;
+ * it has no counterpart there.) It is for callers that cannot allocate device memory: a
+ * plugin that may only use the buffers its host framework hands it, or a loop that must not
+ * call cudaMalloc (which can synchronise the device) between steps. Instead of a workspace,
+ * the per-token partial statistics go to a 16 MiB array built into the library, which every
+ * GPU that loads the library holds until the process exits.
+ *   - Same arguments, outputs and results as hylo_kl_forward, minus the workspace pair.
+ *   - N may be at most 699050 (16 MiB / 24 bytes of statistics per token); larger N returns
+ *     HYLO_ERR_DIM with a message. Smaller N may use fewer vocabulary segments than
+ *     hylo_kl_forward would, which changes results only by fp32 summation order.
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls share the one array per device and it keeps the last call's contents (each call
+ *     writes every slot it reads, so nothing needs clearing). Calls that overlap on the GPU
+ *     (different streams, or threads without ordering) race on it: serialise them. */
+hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16_t* W_s,
+                                    const uint16_t* h_t, const uint16_t* W_t,
+                                    int64_t N, int64_t d_s, int64_t d_t, int64_t V,
+                                    float tau, int64_t token_chunk,
+                                    float* kl, float* lse_s, float* lse_t, float* loss,
+                                    cudaStream_t stream);
+
 /* Synchronises `stream`, then returns and clears the current device's status word:
  * HYLO_OK, or HYLO_ERR_TIMEOUT if a kernel gave up on a pipeline wait since the last read
  * (its outputs are then invalid), or HYLO_ERR_CUDA if the synchronisation failed. */
