@@ -12,7 +12,6 @@ namespace hylo {
 // Tile sizes shared by host and device code.
 constexpr int kBM = 128;      // token rows per tile (UMMA M, one TMEM lane per row)
 constexpr int kBK = 64;       // k elements per pipeline stage (one 128-byte swizzle row)
-constexpr int kFusedBN = 256; // vocab columns per fused tile
 constexpr int kGemmBN = 256;  // output columns per gradient-GEMM tile
 constexpr int kMaxSegments = 32;
 constexpr int kStatFields = 6; // teacher max, teacher sum, student max, student sum, A, C
@@ -43,9 +42,9 @@ struct GemmParams {
   WaitCtl ctl;
 };
 
-int fused_smem_bytes(bool backward);
-cudaError_t fused_prepare(bool backward);
-cudaError_t launch_fused(bool backward, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
+// Fused dual-GEMM kernel; bn = vocabulary columns per tile (256).
+cudaError_t fused_prepare(int bn);
+cudaError_t launch_fused(int bn, bool backward, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
                          const CUtensorMap& Wt, const CUtensorMap& G, const FusedParams& p, int grid,
                          cudaStream_t stream);
 cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, float* kl, float* lse_s,

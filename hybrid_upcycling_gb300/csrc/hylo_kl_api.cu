@@ -49,6 +49,9 @@ hylo_status cuda_fail(cudaError_t e, const char* what) {
   return fail(HYLO_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Vocabulary columns per fused tile (one 128 x 256 teacher + student tile pair fills TMEM).
+constexpr int fused_bn() { return 256; }
+
 unsigned long long wait_limit_ns() {
   static const unsigned long long v = [] {
     const char* s = std::getenv("HYLO_KL_WAIT_LIMIT_MS");
@@ -83,7 +86,7 @@ hylo_status current_device(DeviceState** out) {
       void* p = nullptr;
       if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
       d.status = static_cast<int*>(p);
-      if ((e = fused_prepare(false)) != cudaSuccess || (e = fused_prepare(true)) != cudaSuccess ||
+      if ((e = fused_prepare(fused_bn())) != cudaSuccess ||
           (e = gemm_prepare(false, true)) != cudaSuccess || (e = gemm_prepare(true, true)) != cudaSuccess)
         return cuda_fail(e, "cudaFuncSetAttribute");
       if (!g_encode) {
@@ -206,8 +209,8 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if ((st = make_map(&m_hs, h_s, bf, d_s, N, d_s * 2, kBK, kBM)) != HYLO_OK) return st;
   if ((st = make_map(&m_ht, h_t, bf, d_t, N, d_t * 2, kBK, kBM)) != HYLO_OK) return st;
-  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, kFusedBN)) != HYLO_OK) return st;
-  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, kFusedBN)) != HYLO_OK) return st;
+  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, fused_bn())) != HYLO_OK) return st;
+  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, fused_bn())) != HYLO_OK) return st;
 
   FusedParams p{};
   p.N = static_cast<int>(N);
@@ -215,7 +218,7 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
   p.kb_s = static_cast<int>(cdiv(d_s, kBK));
   p.kb_t = static_cast<int>(cdiv(d_t, kBK));
   p.token_tiles = static_cast<int>(cdiv(N, kBM));
-  p.vtiles = static_cast<int>(cdiv(V, kFusedBN));
+  p.vtiles = static_cast<int>(cdiv(V, fused_bn()));
   p.nseg = choose_segments(p.token_tiles, p.vtiles, dev->sms);
   p.units = p.token_tiles * p.nseg;
   p.c = 1.4426950408889634f / tau;
@@ -224,7 +227,7 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
   const int grid = p.units < dev->sms ? p.units : dev->sms;
 
-  cudaError_t e = launch_fused(false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
+  cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
   e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch combine");
@@ -254,8 +257,8 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
   uint16_t* G = static_cast<uint16_t*>(workspace);
 
   CUtensorMap m_Ws, m_Wt, m_WsB, m_dW;
-  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, kFusedBN)) != HYLO_OK) return st;
-  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, kFusedBN)) != HYLO_OK) return st;
+  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, fused_bn())) != HYLO_OK) return st;
+  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, fused_bn())) != HYLO_OK) return st;
   if ((st = make_map(&m_WsB, W_s, bf, d_s, V, d_s * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major B of dh
   if ((st = make_map(&m_dW, dW_s, f32, d_s, V, d_s * 4, 32, 32)) != HYLO_OK) return st;
 
@@ -281,7 +284,7 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
     p.kb_s = static_cast<int>(cdiv(d_s, kBK));
     p.kb_t = static_cast<int>(cdiv(d_t, kBK));
     p.token_tiles = static_cast<int>(cdiv(R, kBM));
-    p.vtiles = static_cast<int>(cdiv(V, kFusedBN));
+    p.vtiles = static_cast<int>(cdiv(V, fused_bn()));
     p.nseg = choose_segments(p.token_tiles, p.vtiles, dev->sms);
     p.units = p.token_tiles * p.nseg;
     p.c = 1.4426950408889634f / tau;
@@ -291,7 +294,7 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
     p.gscale = gscale;
     p.ctl = ctl;
     int grid = p.units < dev->sms ? p.units : dev->sms;
-    cudaError_t e = launch_fused(true, m_hs, m_Ws, m_ht, m_Wt, m_Gst, p, grid, stream);
+    cudaError_t e = launch_fused(fused_bn(), true, m_hs, m_Ws, m_ht, m_Wt, m_Gst, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launch fused backward");
 
     GemmParams gh{};
@@ -414,8 +417,8 @@ extern "C" hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if ((st = make_map(&m_hs, h_s, bf, d_s, N, d_s * 2, kBK, kBM)) != HYLO_OK) return st;
   if ((st = make_map(&m_ht, h_t, bf, d_t, N, d_t * 2, kBK, kBM)) != HYLO_OK) return st;
-  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, kFusedBN)) != HYLO_OK) return st;
-  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, kFusedBN)) != HYLO_OK) return st;
+  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, fused_bn())) != HYLO_OK) return st;
+  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, fused_bn())) != HYLO_OK) return st;
 
   FusedParams p{};
   p.N = static_cast<int>(N);
@@ -423,7 +426,7 @@ extern "C" hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16
   p.kb_s = static_cast<int>(cdiv(d_s, kBK));
   p.kb_t = static_cast<int>(cdiv(d_t, kBK));
   p.token_tiles = static_cast<int>(cdiv(N, kBM));
-  p.vtiles = static_cast<int>(cdiv(V, kFusedBN));
+  p.vtiles = static_cast<int>(cdiv(V, fused_bn()));
   // as many vocabulary segments as the heuristic wants, but no more than the scratch holds
   const int64_t fit = static_cast<int64_t>(kNoAllocFloats) / (static_cast<int64_t>(kStatFields) * N);
   const int want = choose_segments(p.token_tiles, p.vtiles, dev->sms);
@@ -435,7 +438,7 @@ extern "C" hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
   const int grid = p.units < dev->sms ? p.units : dev->sms;
 
-  cudaError_t e = launch_fused(false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
+  cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
   e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch combine");

@@ -15,9 +15,12 @@
 // next-token distributions, kl_weight 1.0, no cross-entropy (HyLo-Llama-8MLA8GDN-8K-SFT reading
 // notes, kwkr.cn, section "two-stage training recipe", Stage II).
 //
-// Roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues the UMMAs, warps
-// 2..5 are the epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31, so each epilogue
-// thread owns one token row of the 128-row tile and needs no cross-thread reduction.
+// Roles (384 threads, three warpgroups): warp 0 issues TMA loads, warp 1 owns TMEM and issues
+// the UMMAs, warps 2..3 idle; warps 4..11 are the epilogue. Warp w reads TMEM lanes
+// 32*(w%4) .. 32*(w%4)+31, so each epilogue thread owns one token row of the 128-row tile;
+// warps 4..7 take columns 0..127 of the 256-column tile and warps 8..11 columns 128..255. Each epilogue thread first copies its 128
+// teacher logits into registers and releases the teacher accumulator, so the next tile's
+// teacher UMMAs run while the epilogue works on the student half.
 #include <cfloat>
 #include <cmath>
 
@@ -26,23 +29,30 @@
 namespace hylo {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                   // two per TMEM lane quarter, one per column half
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // + TMA warp + UMMA warp
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <bool BWD>
+// BN = vocabulary columns per tile; the 512 TMEM columns hold NBUF = 512 / (2 BN) (teacher,
+// student) tile pairs. Only BN = 256 is instantiated: one pair, drained between tiles (N = 128
+// UMMAs, which would allow two pairs, measured 28% slower end to end on GB300).
+template <int BN_, bool BWD>
 struct FusedCfg {
-  static constexpr int BN = kFusedBN;
+  static constexpr int BN = BN_;
+  static constexpr int HALF = BN / 2;  // columns per epilogue warp
+  static constexpr int NBUF = 512 / (2 * BN);
   static constexpr int A_BYTES = kBM * kBK * 2;
   static constexpr int B_BYTES = BN * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 4;
-  // backward: per epilogue warp two staging buffers of 32 rows x 64 bf16 (128 B rows)
-  static constexpr int STAGING_BYTES = BWD ? 4 * 2 * 32 * 128 : 0;
-  static constexpr int NBUF = 512 / (2 * BN);  // TMEM buffers holding a (teacher, student) tile pair
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES + STAGING_BYTES;
-  static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 1;
+  static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
+  // backward: one staging buffer of 32 rows x 64 bf16 (128 B rows) per epilogue warp;
+  // forward: the statistics of one column half handed to the other half at a unit's end
+  static constexpr int EXTRA_BYTES = BWD ? kEpiWarps * 32 * 128 : kStatFields * kBM * 4;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES + EXTRA_BYTES;
+  // full[S], empty[S], tfull[NBUF], tempty[NBUF], merge_full, merge_empty, drain
+  static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 3;
   static constexpr int SMEM = 1024 + BAR_OFF + NBARS * 8 + 16;
-  static_assert(NBUF >= 1, "TMEM holds at least one tile pair");
+  static_assert(NBUF >= 1 && HALF % 64 == 0, "tile shape");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -70,30 +80,38 @@ struct RowStats {
   float ms, ss;  // student running max, sum_v exp((z_s - ms)/tau)
   float a;       // sum_v exp((z_t - mt)/tau) * d_v, with d_v = (z_t - z_s)/tau
   float cc;      // sum_v exp((z_t - mt)/tau) * (exp(-d_v) - 1 + d_v)   (each term >= 0)
+  bool far;      // exp((m_s - m_t)/tau) overflowed: cc is not valid, the direct KL form is used
 };
 
-// g(d) = exp(-d) - 1 + d for |d| < 1/4 by its Taylor series through d^7 (truncation < 1e-8
+// g(d) = exp(-d) - 1 + d by its Taylor series through d^7, for |d| < 1/4 (truncation < 2e-8
 // relative there); used so that near-identical distributions lose no digits to cancellation.
-__device__ __forceinline__ float g_series(float d) {
-  float t = fmaf(d, -1.0f / 5040.0f, 1.0f / 720.0f);
-  t = fmaf(d, t, -1.0f / 120.0f);
-  t = fmaf(d, t, 1.0f / 24.0f);
-  t = fmaf(d, t, -1.0f / 6.0f);
-  t = fmaf(d, t, 0.5f);
-  return d * d * t;
+__device__ __forceinline__ float2 g_series2(float2 d) {
+  float2 t = __ffma2_rn(d, make_float2(-1.0f / 5040.0f, -1.0f / 5040.0f), make_float2(1.0f / 720.0f, 1.0f / 720.0f));
+  t = __ffma2_rn(d, t, make_float2(-1.0f / 120.0f, -1.0f / 120.0f));
+  t = __ffma2_rn(d, t, make_float2(1.0f / 24.0f, 1.0f / 24.0f));
+  t = __ffma2_rn(d, t, make_float2(-1.0f / 6.0f, -1.0f / 6.0f));
+  t = __ffma2_rn(d, t, make_float2(0.5f, 0.5f));
+  return __fmul2_rn(__fmul2_rn(d, d), t);
 }
 
-// Folds 32 columns of one row into the running statistics. `valid` = number of columns of
-// this chunk that lie inside the vocabulary (32 except in the last tile; MASKED only there).
+__device__ __forceinline__ float2 ex2_approx2(float2 x) { return make_float2(ex2_approx(x.x), ex2_approx(x.y)); }
+
+// Folds 32 columns of one row into the running statistics (column pairs in packed fp32x2
+// arithmetic). `valid` = number of columns of this chunk inside the vocabulary (32 except in
+// the last tile; MASKED only there: masked columns enter as z_t = z_s = max - 2^10 tau, whose
+// exponentials flush to zero and whose d is 0).
+// Each column adds e_t g(d) to C: the Taylor series for |d| < 1/4, otherwise
+// e_t (exp(-d) - 1 + d) = e_s K - e_t + e_t d with K = exp((m_s - m_t)/tau), which uses no
+// extra exponential. K is clamped to stay finite; if the clamp engages the row is marked far.
 template <bool MASKED>
-__device__ __forceinline__ void fold_chunk(RowStats& r, const float (&zt)[32], const float (&zs)[32], int valid,
-                                           float c, float inv_tau) {
+__device__ __forceinline__ void fold_chunk(RowStats& r, const float (&zt_in)[32], const float (&zs_in)[32],
+                                           int valid, float c, float inv_tau) {
   float cmt = -INFINITY, cms = -INFINITY;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     if (!MASKED || j < valid) {
-      cmt = fmaxf(cmt, zt[j]);
-      cms = fmaxf(cms, zs[j]);
+      cmt = fmaxf(cmt, zt_in[j]);
+      cms = fmaxf(cms, zs_in[j]);
     }
   }
   const float nmt = fmaxf(r.mt, cmt);
@@ -106,44 +124,73 @@ __device__ __forceinline__ void fold_chunk(RowStats& r, const float (&zt)[32], c
   r.ss *= as;
   r.mt = nmt;
   r.ms = nms;
-  const float mtc = nmt * c, msc = nms * c;
-  // K = exp((m_s - m_t)/tau) relates student exponentials to the teacher max:
-  // es * K = exp((z_s - m_t)/tau) = et * exp(-d). Clamped so it stays finite; when the clamp
-  // matters the combine step uses the direct formula instead of the cancellation-free one.
-  const float K = ex2_approx(fminf((nms - nmt) * c, 126.0f));
-  float st = 0.f, ss = 0.f, a = 0.f, cc = 0.f;
+  const float kexp = (nms - nmt) * c;
+  r.far = r.far || !(kexp < 126.f);
+  const float K = ex2_approx(fminf(kexp, 126.f));
+  const float2 c2 = make_float2(c, c), it2 = make_float2(inv_tau, inv_tau), m1 = make_float2(-1.f, -1.f);
+  const float2 K2 = make_float2(K, K);
+  const float2 nmtc = make_float2(-nmt * c, -nmt * c), nmsc = make_float2(-nms * c, -nms * c);
+  const float fill = fminf(nmt, nms) - 1024.f / c;  // value of a masked column
+  float2 st = make_float2(0.f, 0.f), ss = st, a = st, cc = st;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const bool ok = !MASKED || j < valid;
-    const float et = ok ? ex2_approx(fmaf(zt[j], c, -mtc)) : 0.f;
-    const float es = ok ? ex2_approx(fmaf(zs[j], c, -msc)) : 0.f;
-    const float d = ok ? (zt[j] - zs[j]) * inv_tau : 0.f;
-    st += et;
-    ss += es;
-    a = fmaf(et, d, a);
-    const float big = fmaf(es, K, fmaf(et, d, -et));
-    cc += (fabsf(d) < 0.25f) ? et * g_series(d) : big;
+  for (int j = 0; j < 16; ++j) {
+    float2 zt = make_float2(zt_in[2 * j], zt_in[2 * j + 1]);
+    float2 zs = make_float2(zs_in[2 * j], zs_in[2 * j + 1]);
+    if (MASKED) {
+      if (2 * j >= valid) zt.x = zs.x = fill;
+      if (2 * j + 1 >= valid) zt.y = zs.y = fill;
+    }
+    const float2 et = ex2_approx2(__ffma2_rn(zt, c2, nmtc));
+    const float2 es = ex2_approx2(__ffma2_rn(zs, c2, nmsc));
+    const float2 d = __fmul2_rn(__ffma2_rn(zs, m1, zt), it2);  // (z_t - z_s) / tau
+    st = __fadd2_rn(st, et);
+    ss = __fadd2_rn(ss, es);
+    const float2 etd = __fmul2_rn(et, d);
+    a = __fadd2_rn(a, etd);
+    const float2 small = __fmul2_rn(et, g_series2(d));
+    const float2 big = __ffma2_rn(es, K2, __ffma2_rn(et, m1, etd));
+    cc = __fadd2_rn(cc, make_float2(fabsf(d.x) < 0.25f ? small.x : big.x, fabsf(d.y) < 0.25f ? small.y : big.y));
   }
-  r.st += st;
-  r.ss += ss;
-  r.a += a;
-  r.cc += cc;
+  r.st += st.x + st.y;
+  r.ss += ss.x + ss.y;
+  r.a += a.x + a.y;
+  r.cc += cc.x + cc.y;
 }
 
-template <bool BWD>
+// Merges the statistics of another set of columns of the same row into `r`. `r` must have
+// seen at least one column; `o` may be empty (maxima -inf, sums 0).
+__device__ __forceinline__ void merge_stats(RowStats& r, const RowStats& o, float c) {
+  const float mt = fmaxf(r.mt, o.mt), ms = fmaxf(r.ms, o.ms);
+  const float wr = ex2_approx((r.mt - mt) * c), wo = ex2_approx((o.mt - mt) * c);
+  const float vr = ex2_approx((r.ms - ms) * c), vo = ex2_approx((o.ms - ms) * c);
+  r.st = r.st * wr + o.st * wo;
+  r.a = r.a * wr + o.a * wo;
+  r.cc = r.cc * wr + o.cc * wo;
+  r.ss = r.ss * vr + o.ss * vo;
+  r.mt = mt;
+  r.ms = ms;
+  r.far = r.far || o.far;
+}
+
+template <int BN_, bool BWD>
 __global__ void __launch_bounds__(kThreads, 1)
 fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant__ CUtensorMap tm_Ws,
                 const __grid_constant__ CUtensorMap tm_ht, const __grid_constant__ CUtensorMap tm_Wt,
                 const __grid_constant__ CUtensorMap tm_G, const FusedParams p) {
-  using C = FusedCfg<BWD>;
+  using C = FusedCfg<BN_, BWD>;
   constexpr int BN = C::BN;
+  constexpr int HALF = C::HALF;
+  constexpr int NBUF = C::NBUF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* extra = smem + C::STAGES * C::STAGE_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* empty = full + C::STAGES;
-  uint64_t* tfull = empty + C::STAGES;
-  uint64_t* tempty = tfull + C::NBUF;
-  uint64_t* drain = tempty + C::NBUF;
+  uint64_t* tfull = empty + C::STAGES;      // UMMA -> epilogue: tile pair in buffer b complete
+  uint64_t* tempty = tfull + NBUF;          // epilogue -> UMMA: buffer b drained
+  uint64_t* merge_full = tempty + NBUF;     // forward: column half 1 -> half 0 statistics handoff
+  uint64_t* merge_empty = merge_full + 1;
+  uint64_t* drain = merge_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -155,10 +202,12 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
-    for (int b = 0; b < C::NBUF; ++b) {
+    for (int b = 0; b < NBUF; ++b) {
       mbar_init(tfull + b, 1);
-      mbar_init(tempty + b, 4);
+      mbar_init(tempty + b, kEpiWarps);
     }
+    mbar_init(merge_full, kEpiWarps / 2);
+    mbar_init(merge_empty, kEpiWarps / 2);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -226,6 +275,8 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ UMMA issuer
+    // Teacher tile (K = d_t) then student tile (K = d_s) into TMEM buffer b: teacher in columns
+    // [2*BN*b, 2*BN*b + BN), student in the next BN columns.
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN, false, false);
       int stage = 0;
@@ -236,8 +287,8 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
         int row0, vt0, vt1, seg;
         unit_range(p, u, row0, vt0, vt1, seg);
         for (int vt = vt0; ok && vt < vt1; ++vt, ++lt) {
-          const int b = lt % C::NBUF;
-          const uint32_t tph = static_cast<uint32_t>(lt / C::NBUF) & 1u;
+          const int b = lt % NBUF;
+          const uint32_t tph = static_cast<uint32_t>(lt / NBUF) & 1u;
           if (!wait_bounded(tempty + b, tph ^ 1u, abort_flag, p.ctl, 2)) {
             ok = false;
             break;
@@ -279,26 +330,28 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
     }
   } else {
     // ------------------------------------------------------------------ epilogue
-    const int q = warp & 3;
-    const int row = q * 32 + lane;
-    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    int lt = 0;
+    const int e = warp - 2;         // 0..7
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int h = e >> 2;           // column half of the tile: [h*128, h*128+128)
+    const int row = q * 32 + lane;  // token row inside the 128-row tile
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * HALF);
+    float* merge = reinterpret_cast<float*>(extra);  // [kStatFields][128]
+    uint8_t* staging = extra + e * 4096;             // backward: 32 rows x 128 B
+    int lt = 0, lu = 0;
     bool ok = true;
-    int sbuf = 0;
-    uint8_t* staging = smem + C::STAGES * C::STAGE_BYTES + (warp - 2) * 2 * 4096;
-    for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x, ++lu) {
       int row0, vt0, vt1, seg;
       unit_range(p, u, row0, vt0, vt1, seg);
       const int token = row0 + row;
-      RowStats rs{-INFINITY, 0.f, -INFINITY, 0.f, 0.f, 0.f};
+      RowStats rs{-INFINITY, 0.f, -INFINITY, 0.f, 0.f, 0.f, false};
       float bt = 0.f, bs = 0.f;
       if (BWD && token < p.N) {
         bt = p.lse_t[token] * kLog2e;
         bs = p.lse_s[token] * kLog2e;
       }
       for (int vt = vt0; vt < vt1; ++vt, ++lt) {
-        const int b = lt % C::NBUF;
-        const uint32_t tph = static_cast<uint32_t>(lt / C::NBUF) & 1u;
+        const int b = lt % NBUF;
+        const uint32_t tph = static_cast<uint32_t>(lt / NBUF) & 1u;
         bool w = wait_bounded(tfull + b, tph, abort_flag, p.ctl, 4);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
@@ -307,15 +360,15 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
         tc_fence_after();
         const uint32_t tT = lane_base + static_cast<uint32_t>(b * 2 * BN);
         const uint32_t tS = tT + BN;
+        const int col_base = vt * BN + h * HALF;
         if (!BWD) {
 #pragma unroll 1
-          for (int ch = 0; ch < BN / 32; ++ch) {
+          for (int c = 0; c < HALF / 32; ++c) {
             float zt[32], zs[32];
-            tmem_ld32(tT + ch * 32, zt);
-            tmem_ld32(tS + ch * 32, zs);
+            tmem_ld32(tT + c * 32, zt);
+            tmem_ld32(tS + c * 32, zs);
             tmem_ld_wait();
-            const int col = vt * BN + ch * 32;
-            const int valid = min(32, p.V - col);
+            const int valid = min(32, p.V - (col_base + c * 32));
             if (valid >= 32) {
               fold_chunk<false>(rs, zt, zs, 32, p.c, p.inv_tau);
             } else if (valid > 0) {
@@ -323,40 +376,42 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
             }
           }
         } else {
+          const uint32_t rowaddr = smem_u32(staging) + lane * 128;
 #pragma unroll 1
-          for (int ch2 = 0; ch2 < BN / 64; ++ch2) {
-            uint8_t* buf = staging + sbuf * 4096;
-            if (lane == 0) bulk_wait_group_read<1>();
-            __syncwarp();
-            const uint32_t rowaddr = smem_u32(buf) + lane * 128;
+          for (int c2 = 0; c2 < HALF / 64; ++c2) {
+            uint32_t pk[2][16];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
+              const int c = c2 * 2 + half;
               float zt[32], zs[32];
-              tmem_ld32(tT + ch2 * 64 + half * 32, zt);
-              tmem_ld32(tS + ch2 * 64 + half * 32, zs);
+              tmem_ld32(tT + c * 32, zt);
+              tmem_ld32(tS + c * 32, zs);
               tmem_ld_wait();
-              uint32_t pk[16];
+              const float2 c2 = make_float2(p.c, p.c), gs2 = make_float2(p.gscale, p.gscale);
+              const float2 nbt = make_float2(-bt, -bt), nbs = make_float2(-bs, -bs), m1 = make_float2(-1.f, -1.f);
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                const float pt0 = ex2_approx(fmaf(zt[2 * j], p.c, -bt));
-                const float ps0 = ex2_approx(fmaf(zs[2 * j], p.c, -bs));
-                const float pt1 = ex2_approx(fmaf(zt[2 * j + 1], p.c, -bt));
-                const float ps1 = ex2_approx(fmaf(zs[2 * j + 1], p.c, -bs));
-                pk[j] = pack_bf16x2((ps0 - pt0) * p.gscale, (ps1 - pt1) * p.gscale);
+                // p_x = exp(z_x / tau - lse_x) = 2^(z_x log2(e) / tau - lse_x log2(e))
+                const float2 pt = ex2_approx2(__ffma2_rn(make_float2(zt[2 * j], zt[2 * j + 1]), c2, nbt));
+                const float2 ps = ex2_approx2(__ffma2_rn(make_float2(zs[2 * j], zs[2 * j + 1]), c2, nbs));
+                const float2 g = __fmul2_rn(__ffma2_rn(pt, m1, ps), gs2);
+                pk[half][j] = pack_bf16x2(g.x, g.y);
               }
+            }
+            if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
+            __syncwarp();
 #pragma unroll
-              for (int c4 = 0; c4 < 4; ++c4) {
-                const uint32_t chunk = static_cast<uint32_t>((half * 4 + c4) ^ (lane & 7));
-                st_shared_v4(rowaddr + chunk * 16, pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
-              }
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const uint32_t chunk = static_cast<uint32_t>(c4 ^ (lane & 7));
+              const uint32_t* src = &pk[c4 >> 2][4 * (c4 & 3)];
+              st_shared_v4(rowaddr + chunk * 16, src[0], src[1], src[2], src[3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tm_G, buf, vt * BN + ch2 * 64, row0 + q * 32);
+              tma_store_2d(&tm_G, staging, col_base + c2 * 64, row0 + q * 32);
               bulk_commit_group();
             }
-            sbuf ^= 1;
           }
         }
         tc_fence_before();
@@ -364,16 +419,41 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
         if (lane == 0) mbar_arrive(tempty + b);
       }
       if (!ok) break;
-      if (!BWD && token < p.N) {
-        const size_t NS = static_cast<size_t>(p.N);
-        float* base = p.part + static_cast<size_t>(seg) * NS + token;
-        const size_t fs = static_cast<size_t>(p.nseg) * NS;  // stride between fields
-        base[0 * fs] = rs.mt;
-        base[1 * fs] = rs.st;
-        base[2 * fs] = rs.ms;
-        base[3 * fs] = rs.ss;
-        base[4 * fs] = rs.a;
-        base[5 * fs] = rs.cc;
+      if (!BWD) {
+        // column half 1 hands its statistics to half 0, which merges and writes them
+        const uint32_t par = static_cast<uint32_t>(lu & 1);
+        if (h == 1) {
+          bool w = wait_bounded(merge_empty, par ^ 1u, abort_flag, p.ctl, 5);
+          if (!__all_sync(0xffffffffu, w)) break;
+          merge[0 * kBM + row] = rs.mt;
+          merge[1 * kBM + row] = rs.st;
+          merge[2 * kBM + row] = rs.ms;
+          merge[3 * kBM + row] = rs.ss;
+          merge[4 * kBM + row] = rs.a;
+          merge[5 * kBM + row] = rs.far ? -1.f : rs.cc;  // cc >= 0 otherwise, so -1 marks "far"
+          __syncwarp();
+          if (lane == 0) mbar_arrive(merge_full);
+        } else {
+          bool w = wait_bounded(merge_full, par, abort_flag, p.ctl, 6);
+          if (!__all_sync(0xffffffffu, w)) break;
+          const float occ = merge[5 * kBM + row];
+          const RowStats o{merge[0 * kBM + row], merge[1 * kBM + row], merge[2 * kBM + row],
+                           merge[3 * kBM + row], merge[4 * kBM + row], occ < 0.f ? 0.f : occ, occ < 0.f};
+          __syncwarp();
+          if (lane == 0) mbar_arrive(merge_empty);
+          merge_stats(rs, o, p.c);
+          if (token < p.N) {
+            const size_t NS = static_cast<size_t>(p.N);
+            float* base = p.part + static_cast<size_t>(seg) * NS + token;
+            const size_t fs = static_cast<size_t>(p.nseg) * NS;  // stride between fields
+            base[0 * fs] = rs.mt;
+            base[1 * fs] = rs.st;
+            base[2 * fs] = rs.ms;
+            base[3 * fs] = rs.ss;
+            base[4 * fs] = rs.a;
+            base[5 * fs] = rs.far ? -1.f : rs.cc;
+          }
+        }
       }
     }
     if (BWD && lane == 0) bulk_wait_group<0>();
@@ -388,8 +468,9 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
 }
 
 // Merges the per-segment statistics of each token (fp64) and writes kl, lse_s, lse_t.
-// KL = A/S_t - lse_t + lse_s in general; when the two distributions are close the algebraically
-// equal form KL = C' + log1p(C' - mu) - (C' - mu), with mu = A/S_t = E_pt[d] and
+// KL = A/S_t - lse_t + lse_s in general; when C is valid (marked by C >= 0) and the two
+// distributions are close, the algebraically equal form
+// KL = C' + log1p(C' - mu) - (C' - mu), with mu = A/S_t = E_pt[d] and
 // C' = C/S_t = E_pt[exp(-d) - 1 + d] >= 0, avoids the cancellation of two ~log V terms.
 __global__ void kl_combine_kernel(const float* __restrict__ part, int N, int nseg, float inv_tau,
                                   float* __restrict__ kl, float* __restrict__ lse_s, float* __restrict__ lse_t) {
@@ -404,14 +485,17 @@ __global__ void kl_combine_kernel(const float* __restrict__ part, int N, int nse
     Ms = fmax(Ms, static_cast<double>(b[2 * fs + s * NS]));
   }
   double St = 0, Ss = 0, A = 0, Cc = 0;
+  bool far = false;
   const double it = inv_tau;
   for (int s = 0; s < nseg; ++s) {
     const double mt = b[s * NS], ms = b[2 * fs + s * NS];
     const double wt = (mt == -INFINITY) ? 0.0 : exp((mt - Mt) * it);
     const double ws = (ms == -INFINITY) ? 0.0 : exp((ms - Ms) * it);
+    const double cs = b[5 * fs + s * NS];
     St += wt * b[fs + s * NS];
     A += wt * b[4 * fs + s * NS];
-    Cc += wt * b[5 * fs + s * NS];
+    far = far || cs < 0.0;
+    Cc += wt * cs;
     Ss += ws * b[3 * fs + s * NS];
   }
   const double lt = Mt * it + log(St);
@@ -420,7 +504,7 @@ __global__ void kl_combine_kernel(const float* __restrict__ part, int N, int nse
   const double cn = Cc / St;
   const double u = cn - mu;
   double k;
-  if (isfinite(u) && fabs(u) < 0.5) {
+  if (!far && isfinite(u) && fabs(u) < 0.5) {
     k = cn + (log1p(u) - u);
   } else {
     k = mu - lt + ls;
@@ -444,27 +528,34 @@ __global__ void __launch_bounds__(1024) kl_mean_kernel(const float* __restrict__
   if (threadIdx.x == 0) loss[0] = static_cast<float>(red[0] / static_cast<double>(N));
 }
 
-}  // namespace
-
-int fused_smem_bytes(bool backward) { return backward ? FusedCfg<true>::SMEM : FusedCfg<false>::SMEM; }
-
-cudaError_t fused_prepare(bool backward) {
-  if (backward)
-    return cudaFuncSetAttribute(fused_kl_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                FusedCfg<true>::SMEM);
-  return cudaFuncSetAttribute(fused_kl_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              FusedCfg<false>::SMEM);
+template <int BN, bool BWD>
+cudaError_t prepare_one() {
+  return cudaFuncSetAttribute(fused_kl_kernel<BN, BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              FusedCfg<BN, BWD>::SMEM);
 }
 
-cudaError_t launch_fused(bool backward, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
+template <int BN, bool BWD>
+cudaError_t launch_one(const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht, const CUtensorMap& Wt,
+                       const CUtensorMap& G, const FusedParams& p, int grid, cudaStream_t stream) {
+  fused_kl_kernel<BN, BWD><<<grid, kThreads, FusedCfg<BN, BWD>::SMEM, stream>>>(hs, Ws, ht, Wt, G, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t fused_prepare(int bn) {
+  if (bn != 256) return cudaErrorInvalidValue;
+  cudaError_t e;
+  if ((e = prepare_one<256, false>()) != cudaSuccess) return e;
+  return prepare_one<256, true>();
+}
+
+cudaError_t launch_fused(int bn, bool backward, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
                          const CUtensorMap& Wt, const CUtensorMap& G, const FusedParams& p, int grid,
                          cudaStream_t stream) {
-  if (backward) {
-    fused_kl_kernel<true><<<grid, kThreads, FusedCfg<true>::SMEM, stream>>>(hs, Ws, ht, Wt, G, p);
-  } else {
-    fused_kl_kernel<false><<<grid, kThreads, FusedCfg<false>::SMEM, stream>>>(hs, Ws, ht, Wt, G, p);
-  }
-  return cudaGetLastError();
+  if (bn != 256) return cudaErrorInvalidValue;
+  return backward ? launch_one<256, true>(hs, Ws, ht, Wt, G, p, grid, stream)
+                  : launch_one<256, false>(hs, Ws, ht, Wt, G, p, grid, stream);
 }
 
 cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, float* kl, float* lse_s,

@@ -146,6 +146,19 @@ def test_identical_student_and_teacher_give_exact_zero():
     assert torch.equal(g["lse_s"], g["lse_t"])
 
 
+def test_single_outlier_vocab_row():
+    """Teacher = student except one vocabulary row: d = 0 on every other column and O(1) on that
+    one, so the KL is small while some |d| is large (both branches of the cancellation-free
+    sum, and the mean-loss bound at a small loss)."""
+    x = gen(500, 128, 128, 4000, seed=21, w_std=0.1)
+    x["h_t"] = x["h_s"].clone()
+    Wt = x["W_s"].clone()
+    Wt[7] = (Wt[7].float() + 0.03 * torch.randn(128, device="cuda", generator=torch.Generator("cuda").manual_seed(5))).to(torch.bfloat16)
+    x["W_t"] = Wt
+    g = check_dense(x, 1.0, 256)
+    assert 0 < g["loss"].item() < 1e-2
+
+
 def test_near_converged_cancellation():
     """Student logits = teacher logits + 1e-2-scale noise: KL ~ 7e-5 from two ~log V terms."""
     w = syn.WORKLOADS["llama3b_nearconv"].with_sizes(N=700, V=6000)
