@@ -167,7 +167,7 @@ def step(w, x, b, stream, ev=None):
 
 def launches_per_step(w) -> int:
     chunks = math.ceil(w.N / min(w.token_chunk, w.N))
-    return 3 + 3 * chunks  # fused fwd + combine + mean; per chunk: fused G + dh GEMM + dW GEMM
+    return 3 + 2 * chunks  # fused fwd + combine + mean; per chunk: fused G + paired dh/dW GEMM
 
 
 def cpu_oracle_rate(w, x, sample_tokens: int, repeats: int = 1):

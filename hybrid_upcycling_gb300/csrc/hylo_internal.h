@@ -34,11 +34,24 @@ struct FusedParams {
   WaitCtl ctl;
 };
 
-// Parameters of the dense gradient GEMM C[M, Nc] (=|+=) sum_k A[m, k] B[n, k].
+// One GEMM problem C[M, Nc] (=|+=) sum_k A[m, k] B[n, k] of the paired gradient kernel, tiled
+// in 256 x 256 pair tiles (each CTA of a pair owns 128 rows of the tile).
+struct GemmProblem {
+  int M, Nc;
+  int kblocks;               // ceil(K / 64)
+  int m_tiles, n_tiles, tiles;
+  int a_mn;                  // A operand MN-major (1) or K-major (0); B is MN-major
+  int accumulate;            // 0: overwrite C, 1: add into C (TMA reduce-add)
+};
+
+constexpr int kMaxClusters = 128;
+
+// Both gradient problems of one token chunk: problem 0 (dh_s) tiles are dealt round-robin over
+// the clusters, problem 1 (dW_s) tiles [p1_begin[c], p1_begin[c + 1]) go to cluster c.
 struct GemmParams {
-  int M, Nc, K;
-  int m_tiles, n_tiles, kblocks, tiles;
-  int accumulate;   // 0: overwrite C, 1: add into C (TMA reduce-add)
+  GemmProblem prob[2];
+  int nclusters;
+  int p1_begin[kMaxClusters + 1];
   WaitCtl ctl;
 };
 
@@ -51,10 +64,11 @@ cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, fl
                            float* lse_t, cudaStream_t stream);
 cudaError_t launch_mean(const float* kl, int N, float* loss, cudaStream_t stream);
 
-// A and B are K-major (false) or MN-major (true).
+// Paired (cta_group::2) gradient GEMM: sets the shared-memory limit and reports how many
+// 2-CTA clusters fit on the device at once; the launch runs p.nclusters clusters.
 int gemm_smem_bytes();
-cudaError_t gemm_prepare(bool a_mn, bool b_mn);
-cudaError_t launch_gemm(bool a_mn, bool b_mn, const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& C,
-                        const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t gemm_prepare(int* max_clusters);
+cudaError_t launch_gemm_pair(const CUtensorMap& A0, const CUtensorMap& B0, const CUtensorMap& C0, const CUtensorMap& A1,
+                             const CUtensorMap& B1, const CUtensorMap& C1, const GemmParams& p, cudaStream_t stream);
 
 }  // namespace hylo

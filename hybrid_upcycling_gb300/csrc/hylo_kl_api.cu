@@ -27,6 +27,7 @@ struct DeviceState {
   bool init = false;
   bool sm103 = false;
   int sms = 0;
+  int gemm_clusters = 0;  // 2-CTA clusters of the gradient GEMM resident at once
   int* status = nullptr;
   std::string why;
 };
@@ -86,9 +87,10 @@ hylo_status current_device(DeviceState** out) {
       void* p = nullptr;
       if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
       d.status = static_cast<int*>(p);
-      if ((e = fused_prepare(fused_bn())) != cudaSuccess ||
-          (e = gemm_prepare(false, true)) != cudaSuccess || (e = gemm_prepare(true, true)) != cudaSuccess)
-        return cuda_fail(e, "cudaFuncSetAttribute");
+      if ((e = fused_prepare(fused_bn())) != cudaSuccess || (e = gemm_prepare(&d.gemm_clusters)) != cudaSuccess)
+        return cuda_fail(e, "kernel set-up");
+      if (d.gemm_clusters < 1) return fail(HYLO_ERR_CUDA, "no 2-CTA cluster of the gradient GEMM fits on the device");
+      if (d.gemm_clusters > kMaxClusters) d.gemm_clusters = kMaxClusters;
       if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
         void* fn = nullptr;
@@ -159,6 +161,45 @@ int choose_segments(int64_t token_tiles, int64_t vtiles, int sms) {
     }
   }
   return best;
+}
+
+// Balanced static schedule of the paired gradient GEMM: problem-0 tiles (long, K = V) go
+// round-robin; each cluster then gets a count of problem-1 tiles (short) chosen so that every
+// cluster's total k-blocks reach the smallest common finish time, as contiguous ranges.
+void schedule_gemm(GemmParams& gp) {
+  const int ncl = gp.nclusters;
+  const int64_t t0 = gp.prob[0].tiles, t1 = gp.prob[1].tiles;
+  const int64_t k0 = gp.prob[0].kblocks, k1 = gp.prob[1].kblocks > 0 ? gp.prob[1].kblocks : 1;
+  int64_t load[kMaxClusters], w[kMaxClusters];
+  int64_t maxload = 0;
+  for (int c = 0; c < ncl; ++c) {
+    load[c] = (t0 > c ? (t0 - 1 - c) / ncl + 1 : 0) * k0;
+    if (load[c] > maxload) maxload = load[c];
+  }
+  auto fill = [&](int64_t T) {
+    int64_t n = 0;
+    for (int c = 0; c < ncl; ++c) n += T > load[c] ? (T - load[c]) / k1 : 0;
+    return n;
+  };
+  int64_t lo = 0, hi = maxload + (t1 / ncl + 2) * k1;
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (fill(mid) >= t1) hi = mid; else lo = mid + 1;
+  }
+  int64_t sum = 0;
+  for (int c = 0; c < ncl; ++c) {
+    w[c] = lo > load[c] ? (lo - load[c]) / k1 : 0;
+    sum += w[c];
+  }
+  while (sum > t1) {  // remove the excess from the clusters that would finish last
+    int cmax = -1;
+    for (int c = 0; c < ncl; ++c)
+      if (w[c] > 0 && (cmax < 0 || load[c] + w[c] * k1 > load[cmax] + w[cmax] * k1)) cmax = c;
+    --w[cmax];
+    --sum;
+  }
+  gp.p1_begin[0] = 0;
+  for (int c = 0; c < ncl; ++c) gp.p1_begin[c + 1] = gp.p1_begin[c] + static_cast<int>(w[c]);
 }
 
 hylo_status check_common(const void* h_s, const void* W_s, const void* h_t, const void* W_t, int64_t N, int64_t d_s,
@@ -297,33 +338,31 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
     cudaError_t e = launch_fused(fused_bn(), true, m_hs, m_Ws, m_ht, m_Wt, m_Gst, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launch fused backward");
 
-    GemmParams gh{};
-    gh.M = static_cast<int>(R);
-    gh.Nc = static_cast<int>(d_s);
-    gh.K = static_cast<int>(V);
-    gh.m_tiles = static_cast<int>(cdiv(R, kBM));
-    gh.n_tiles = static_cast<int>(cdiv(d_s, kGemmBN));
-    gh.kblocks = static_cast<int>(cdiv(V, kBK));
-    gh.tiles = gh.m_tiles * gh.n_tiles;
-    gh.accumulate = 0;
-    gh.ctl = ctl;
-    grid = gh.tiles < dev->sms ? gh.tiles : dev->sms;
-    e = launch_gemm(false, true, m_GA, m_WsB, m_dh, gh, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "launch dh GEMM");
-
-    GemmParams gw{};
-    gw.M = static_cast<int>(V);
-    gw.Nc = static_cast<int>(d_s);
-    gw.K = static_cast<int>(R);
-    gw.m_tiles = static_cast<int>(cdiv(V, kBM));
-    gw.n_tiles = static_cast<int>(cdiv(d_s, kGemmBN));
-    gw.kblocks = static_cast<int>(cdiv(R, kBK));
-    gw.tiles = gw.m_tiles * gw.n_tiles;
-    gw.accumulate = c0 > 0 ? 1 : 0;
-    gw.ctl = ctl;
-    grid = gw.tiles < dev->sms ? gw.tiles : dev->sms;
-    e = launch_gemm(true, true, m_GT, m_hsB, m_dW, gw, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "launch dW GEMM");
+    GemmParams gp{};
+    GemmProblem& dh = gp.prob[0];
+    dh.M = static_cast<int>(R);
+    dh.Nc = static_cast<int>(d_s);
+    dh.kblocks = static_cast<int>(cdiv(V, kBK));
+    dh.m_tiles = static_cast<int>(cdiv(R, 2 * kBM));
+    dh.n_tiles = static_cast<int>(cdiv(d_s, kGemmBN));
+    dh.tiles = dh.m_tiles * dh.n_tiles;
+    dh.a_mn = 0;
+    dh.accumulate = 0;
+    GemmProblem& dw = gp.prob[1];
+    dw.M = static_cast<int>(V);
+    dw.Nc = static_cast<int>(d_s);
+    dw.kblocks = static_cast<int>(cdiv(R, kBK));
+    dw.m_tiles = static_cast<int>(cdiv(V, 2 * kBM));
+    dw.n_tiles = static_cast<int>(cdiv(d_s, kGemmBN));
+    dw.tiles = dw.m_tiles * dw.n_tiles;
+    dw.a_mn = 1;
+    dw.accumulate = c0 > 0 ? 1 : 0;
+    const int64_t all_tiles = static_cast<int64_t>(dh.tiles) + dw.tiles;
+    gp.nclusters = static_cast<int>(all_tiles < dev->gemm_clusters ? all_tiles : dev->gemm_clusters);
+    gp.ctl = ctl;
+    schedule_gemm(gp);
+    e = launch_gemm_pair(m_GA, m_WsB, m_dh, m_GT, m_hsB, m_dW, gp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launch gradient GEMM");
   }
   return HYLO_OK;
 }
