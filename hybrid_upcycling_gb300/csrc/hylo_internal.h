@@ -12,7 +12,8 @@ namespace hylo {
 // Tile sizes shared by host and device code.
 constexpr int kBM = 128;      // token rows per tile (UMMA M, one TMEM lane per row)
 constexpr int kBK = 64;       // k elements per pipeline stage (one 128-byte swizzle row)
-constexpr int kGemmBN = 256;  // output columns per gradient-GEMM tile
+constexpr int kGemmBN = 256;  // output columns per gradient-GEMM pair tile
+constexpr int kFusedBN = 256; // vocabulary columns per fused pair tile (each CTA stages 128 W rows)
 constexpr int kMaxSegments = 32;
 constexpr int kStatFields = 6; // teacher max, teacher sum, student max, student sum, A, C
 
@@ -21,9 +22,9 @@ struct FusedParams {
   int N;            // token rows covered by the tensor maps of this launch
   int V;            // vocabulary size
   int kb_s, kb_t;   // 64-wide k-blocks of the student / teacher projections
-  int token_tiles;  // ceil(N / 128)
-  int vtiles;       // ceil(V / BN)
-  int nseg;         // vocabulary segments per token tile
+  int token_tiles;  // ceil(N / 256): 256-token pair tiles
+  int vtiles;       // ceil(V / kFusedBN)
+  int nseg;         // vocabulary segments per pair tile
   int units;        // token_tiles * nseg
   float c;          // log2(e) / tau
   float inv_tau;    // 1 / tau
@@ -55,10 +56,12 @@ struct GemmParams {
   WaitCtl ctl;
 };
 
-// Fused dual-GEMM kernel; bn = vocabulary columns per tile (256).
-cudaError_t fused_prepare(int bn);
+// Fused dual-GEMM kernel on CTA pairs; bn = vocabulary columns per pair tile (kFusedBN).
+// fused_prepare reports how many 2-CTA clusters fit on the device at once; a launch runs
+// `clusters` clusters, each working through units (256-token tile, vocabulary segment).
+cudaError_t fused_prepare(int bn, int* max_clusters);
 cudaError_t launch_fused(int bn, bool backward, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
-                         const CUtensorMap& Wt, const CUtensorMap& G, const FusedParams& p, int grid,
+                         const CUtensorMap& Wt, const CUtensorMap& G, const FusedParams& p, int clusters,
                          cudaStream_t stream);
 cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, float* kl, float* lse_s,
                            float* lse_t, cudaStream_t stream);

@@ -27,7 +27,8 @@ struct DeviceState {
   bool init = false;
   bool sm103 = false;
   int sms = 0;
-  int gemm_clusters = 0;  // 2-CTA clusters of the gradient GEMM resident at once
+  int gemm_clusters = 0;   // 2-CTA clusters of the gradient GEMM resident at once
+  int fused_clusters = 0;  // 2-CTA clusters of the fused kernels resident at once
   int* status = nullptr;
   std::string why;
 };
@@ -50,8 +51,8 @@ hylo_status cuda_fail(cudaError_t e, const char* what) {
   return fail(HYLO_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// Vocabulary columns per fused tile (one 128 x 256 teacher + student tile pair fills TMEM).
-constexpr int fused_bn() { return 256; }
+// Vocabulary columns per fused pair tile.
+constexpr int fused_bn() { return kFusedBN; }
 
 unsigned long long wait_limit_ns() {
   static const unsigned long long v = [] {
@@ -87,9 +88,11 @@ hylo_status current_device(DeviceState** out) {
       void* p = nullptr;
       if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
       d.status = static_cast<int*>(p);
-      if ((e = fused_prepare(fused_bn())) != cudaSuccess || (e = gemm_prepare(&d.gemm_clusters)) != cudaSuccess)
+      if ((e = fused_prepare(fused_bn(), &d.fused_clusters)) != cudaSuccess ||
+          (e = gemm_prepare(&d.gemm_clusters)) != cudaSuccess)
         return cuda_fail(e, "kernel set-up");
-      if (d.gemm_clusters < 1) return fail(HYLO_ERR_CUDA, "no 2-CTA cluster of the gradient GEMM fits on the device");
+      if (d.gemm_clusters < 1 || d.fused_clusters < 1)
+        return fail(HYLO_ERR_CUDA, "no 2-CTA cluster of the kernels fits on the device");
       if (d.gemm_clusters > kMaxClusters) d.gemm_clusters = kMaxClusters;
       if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
@@ -144,15 +147,15 @@ size_t bwd_bytes(int64_t N, int64_t V, int64_t token_chunk) {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Number of vocabulary segments per token tile: the work units (token tile, segment) are dealt
-// round-robin to one persistent CTA per SM, so pick the split that minimises
+// Number of vocabulary segments per pair tile: the work units (256-token tile, segment) are
+// dealt round-robin to the persistent CTA pairs, so pick the split that minimises
 // waves x (vocab tiles per segment), with a small cost per extra segment.
-int choose_segments(int64_t token_tiles, int64_t vtiles, int sms) {
+int choose_segments(int64_t token_tiles, int64_t vtiles, int workers) {
   int best = 1;
   double best_cost = 1e300;
   for (int s = 1; s <= kMaxSegments && s <= vtiles; ++s) {
     const int64_t units = token_tiles * s;
-    const int64_t waves = cdiv(units, sms);
+    const int64_t waves = cdiv(units, workers);
     const int64_t per = cdiv(vtiles, s);
     const double cost = static_cast<double>(waves * per) * (1.0 + 0.002 * s);
     if (cost < best_cost) {
@@ -250,23 +253,23 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if ((st = make_map(&m_hs, h_s, bf, d_s, N, d_s * 2, kBK, kBM)) != HYLO_OK) return st;
   if ((st = make_map(&m_ht, h_t, bf, d_t, N, d_t * 2, kBK, kBM)) != HYLO_OK) return st;
-  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, fused_bn())) != HYLO_OK) return st;
-  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, fused_bn())) != HYLO_OK) return st;
+  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, fused_bn() / 2)) != HYLO_OK) return st;
+  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, fused_bn() / 2)) != HYLO_OK) return st;
 
   FusedParams p{};
   p.N = static_cast<int>(N);
   p.V = static_cast<int>(V);
   p.kb_s = static_cast<int>(cdiv(d_s, kBK));
   p.kb_t = static_cast<int>(cdiv(d_t, kBK));
-  p.token_tiles = static_cast<int>(cdiv(N, kBM));
+  p.token_tiles = static_cast<int>(cdiv(N, 2 * kBM));
   p.vtiles = static_cast<int>(cdiv(V, fused_bn()));
-  p.nseg = choose_segments(p.token_tiles, p.vtiles, dev->sms);
+  p.nseg = choose_segments(p.token_tiles, p.vtiles, dev->fused_clusters);
   p.units = p.token_tiles * p.nseg;
   p.c = 1.4426950408889634f / tau;
   p.inv_tau = 1.0f / tau;
   p.part = static_cast<float*>(workspace);
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
-  const int grid = p.units < dev->sms ? p.units : dev->sms;
+  const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
 
   cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
@@ -298,8 +301,8 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
   uint16_t* G = static_cast<uint16_t*>(workspace);
 
   CUtensorMap m_Ws, m_Wt, m_WsB, m_dW;
-  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, fused_bn())) != HYLO_OK) return st;
-  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, fused_bn())) != HYLO_OK) return st;
+  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, fused_bn() / 2)) != HYLO_OK) return st;
+  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, fused_bn() / 2)) != HYLO_OK) return st;
   if ((st = make_map(&m_WsB, W_s, bf, d_s, V, d_s * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major B of dh
   if ((st = make_map(&m_dW, dW_s, f32, d_s, V, d_s * 4, 32, 32)) != HYLO_OK) return st;
 
@@ -324,9 +327,9 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
     p.V = static_cast<int>(V);
     p.kb_s = static_cast<int>(cdiv(d_s, kBK));
     p.kb_t = static_cast<int>(cdiv(d_t, kBK));
-    p.token_tiles = static_cast<int>(cdiv(R, kBM));
+    p.token_tiles = static_cast<int>(cdiv(R, 2 * kBM));
     p.vtiles = static_cast<int>(cdiv(V, fused_bn()));
-    p.nseg = choose_segments(p.token_tiles, p.vtiles, dev->sms);
+    p.nseg = choose_segments(p.token_tiles, p.vtiles, dev->fused_clusters);
     p.units = p.token_tiles * p.nseg;
     p.c = 1.4426950408889634f / tau;
     p.inv_tau = 1.0f / tau;
@@ -334,7 +337,7 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
     p.lse_t = lse_t + c0;
     p.gscale = gscale;
     p.ctl = ctl;
-    int grid = p.units < dev->sms ? p.units : dev->sms;
+    const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
     cudaError_t e = launch_fused(fused_bn(), true, m_hs, m_Ws, m_ht, m_Wt, m_Gst, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launch fused backward");
 
@@ -456,26 +459,26 @@ extern "C" hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if ((st = make_map(&m_hs, h_s, bf, d_s, N, d_s * 2, kBK, kBM)) != HYLO_OK) return st;
   if ((st = make_map(&m_ht, h_t, bf, d_t, N, d_t * 2, kBK, kBM)) != HYLO_OK) return st;
-  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, fused_bn())) != HYLO_OK) return st;
-  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, fused_bn())) != HYLO_OK) return st;
+  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, fused_bn() / 2)) != HYLO_OK) return st;
+  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, fused_bn() / 2)) != HYLO_OK) return st;
 
   FusedParams p{};
   p.N = static_cast<int>(N);
   p.V = static_cast<int>(V);
   p.kb_s = static_cast<int>(cdiv(d_s, kBK));
   p.kb_t = static_cast<int>(cdiv(d_t, kBK));
-  p.token_tiles = static_cast<int>(cdiv(N, kBM));
+  p.token_tiles = static_cast<int>(cdiv(N, 2 * kBM));
   p.vtiles = static_cast<int>(cdiv(V, fused_bn()));
   // as many vocabulary segments as the heuristic wants, but no more than the scratch holds
   const int64_t fit = static_cast<int64_t>(kNoAllocFloats) / (static_cast<int64_t>(kStatFields) * N);
-  const int want = choose_segments(p.token_tiles, p.vtiles, dev->sms);
+  const int want = choose_segments(p.token_tiles, p.vtiles, dev->fused_clusters);
   p.nseg = static_cast<int>(want < fit ? want : fit);
   p.units = p.token_tiles * p.nseg;
   p.c = 1.4426950408889634f / tau;
   p.inv_tau = 1.0f / tau;
   p.part = scratch;  // every (segment, token) slot read by the combine step is written first
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
-  const int grid = p.units < dev->sms ? p.units : dev->sms;
+  const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
 
   cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");

@@ -33,16 +33,20 @@ constexpr int kEpiWarps = 8;                   // two per TMEM lane quarter, one
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // + TMA warp + UMMA warp
 constexpr float kLog2e = 1.4426950408889634f;
 
-// BN = vocabulary columns per tile; the 512 TMEM columns hold NBUF = 512 / (2 BN) (teacher,
-// student) tile pairs. Only BN = 256 is instantiated: one pair, drained between tiles (N = 128
-// UMMAs, which would allow two pairs, measured 28% slower end to end on GB300).
+// A CTA pair (cluster of 2 on an SM pair) computes a 256-token x BN-word tile with one
+// tcgen05.mma.cta_group::2 per 16-deep slice (M = 256): each CTA stages its 128 token rows of
+// h and BN/2 rows of W, and each CTA's TMEM holds its 128 rows of the teacher and student
+// tiles. kFusedBN = 256: one (teacher, student) pair fills the 512 TMEM columns and is drained
+// between tiles. (BN = 128 would fit two pairs and overlap the epilogue with the next tile's
+// UMMAs, but N = 128 UMMAs measured 22% slower end to end on GB300, on one CTA or on a pair.)
 template <int BN_, bool BWD>
 struct FusedCfg {
-  static constexpr int BN = BN_;
-  static constexpr int HALF = BN / 2;  // columns per epilogue warp
+  static constexpr int BN = BN_;         // vocabulary columns per pair tile
+  static constexpr int HB = BN / 2;      // W rows staged per CTA
+  static constexpr int HALF = BN / 2;    // columns per epilogue warp
   static constexpr int NBUF = 512 / (2 * BN);
   static constexpr int A_BYTES = kBM * kBK * 2;
-  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int B_BYTES = HB * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
   // backward: one staging buffer of 32 rows x 64 bf16 (128 B rows) per epilogue warp;
@@ -52,7 +56,7 @@ struct FusedCfg {
   // full[S], empty[S], tfull[NBUF], tempty[NBUF], merge_full, merge_empty, drain
   static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 3;
   static constexpr int SMEM = 1024 + BAR_OFF + NBARS * 8 + 16;
-  static_assert(NBUF >= 1 && HALF % 64 == 0, "tile shape");
+  static_assert(NBUF >= 1 && HALF % 64 == 0 && HB % 8 == 0, "tile shape");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -65,10 +69,11 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsig
   }
 }
 
+// Work unit u = (256-token pair tile, vocabulary segment); row0 = the pair tile's first token.
 __device__ __forceinline__ void unit_range(const FusedParams& p, int u, int& row0, int& vt0, int& vt1, int& seg) {
   const int ti = u / p.nseg;
   seg = u - ti * p.nseg;
-  row0 = ti * kBM;
+  row0 = ti * 2 * kBM;
   vt0 = static_cast<int>((static_cast<long long>(seg) * p.vtiles) / p.nseg);
   vt1 = static_cast<int>((static_cast<long long>(seg + 1) * p.vtiles) / p.nseg);
 }
@@ -179,15 +184,16 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
                 const __grid_constant__ CUtensorMap tm_G, const FusedParams p) {
   using C = FusedCfg<BN_, BWD>;
   constexpr int BN = C::BN;
+  constexpr int HB = C::HB;
   constexpr int HALF = C::HALF;
   constexpr int NBUF = C::NBUF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* extra = smem + C::STAGES * C::STAGE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* empty = full + C::STAGES;
-  uint64_t* tfull = empty + C::STAGES;      // UMMA -> epilogue: tile pair in buffer b complete
-  uint64_t* tempty = tfull + NBUF;          // epilogue -> UMMA: buffer b drained
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);  // used in the even CTA
+  uint64_t* empty = full + C::STAGES;       // both CTAs: stage free (UMMAs done reading it)
+  uint64_t* tfull = empty + C::STAGES;      // both CTAs: tile pair in TMEM buffer b complete
+  uint64_t* tempty = tfull + NBUF;          // even CTA: buffer b drained by both epilogues
   uint64_t* merge_full = tempty + NBUF;     // forward: column half 1 -> half 0 statistics handoff
   uint64_t* merge_empty = merge_full + 1;
   uint64_t* drain = merge_empty + 1;
@@ -196,6 +202,9 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the UMMAs
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -204,7 +213,7 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
     }
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(tfull + b, 1);
-      mbar_init(tempty + b, kEpiWarps);
+      mbar_init(tempty + b, 2 * kEpiWarps);  // every epilogue warp of both CTAs
     }
     mbar_init(merge_full, kEpiWarps / 2);
     mbar_init(merge_empty, kEpiWarps / 2);
@@ -220,27 +229,30 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
     if (BWD) prefetch_tmap(&tm_G);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int kbt = p.kb_t, kbtot = p.kb_t + p.kb_s;
+  const int my_rows = static_cast<int>(rank) * kBM;  // this CTA's token rows inside a pair tile
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed = 0;  // bit s: stage s has been armed at least once
+      uint32_t armed = 0;  // bit s: stage s has been armed at least once (even CTA)
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+      for (int u = cid; ok && u < p.units; u += ncl) {
         int row0, vt0, vt1, seg;
         unit_range(p, u, row0, vt0, vt1, seg);
+        const int arow = row0 + my_rows;
         for (int vt = vt0; ok && vt < vt1; ++vt) {
-          const int col0 = vt * BN;
+          const int brow = vt * BN + static_cast<int>(rank) * HB;
           for (int kb = 0; kb < kbtot; ++kb) {
             if (!wait_bounded(empty + stage, phase ^ 1u, abort_flag, p.ctl, 1)) {
               ok = false;
@@ -248,15 +260,18 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
             }
             uint8_t* sa = smem + stage * C::STAGE_BYTES;
             uint8_t* sb = sa + C::A_BYTES;
-            mbar_arrive_expect_tx(full + stage, C::STAGE_BYTES);
-            armed |= 1u << stage;
+            const uint32_t fbar = mapa_shared(smem_u32(full + stage), 0);
+            if (rank == 0) {
+              mbar_arrive_expect_tx(full + stage, 2 * C::STAGE_BYTES);  // both CTAs' bytes
+              armed |= 1u << stage;
+            }
             if (kb < kbt) {
-              tma_load_2d(sa, &tm_ht, full + stage, kb * kBK, row0);
-              tma_load_2d(sb, &tm_Wt, full + stage, kb * kBK, col0);
+              tma_load_2d_pair(sa, &tm_ht, fbar, kb * kBK, arow);
+              tma_load_2d_pair(sb, &tm_Wt, fbar, kb * kBK, brow);
             } else {
               const int k = kb - kbt;
-              tma_load_2d(sa, &tm_hs, full + stage, k * kBK, row0);
-              tma_load_2d(sb, &tm_Ws, full + stage, k * kBK, col0);
+              tma_load_2d_pair(sa, &tm_hs, fbar, k * kBK, arow);
+              tma_load_2d_pair(sb, &tm_Ws, fbar, k * kBK, brow);
             }
             if (++stage == C::STAGES) {
               stage = 0;
@@ -274,16 +289,16 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ UMMA issuer
-    // Teacher tile (K = d_t) then student tile (K = d_s) into TMEM buffer b: teacher in columns
-    // [2*BN*b, 2*BN*b + BN), student in the next BN columns.
-    if (lane == 0) {
-      constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN, false, false);
+    // ------------------------------------------------------------------ UMMA issuer (even CTA)
+    // Teacher tile (K = d_t) then student tile (K = d_s) into TMEM buffer b of both CTAs:
+    // teacher in columns [2*BN*b, 2*BN*b + BN), student in the next BN columns.
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, BN, false, false);
       int stage = 0;
       uint32_t phase = 0;
       int lt = 0;
       bool ok = true, issued = false;
-      for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+      for (int u = cid; ok && u < p.units; u += ncl) {
         int row0, vt0, vt1, seg;
         unit_range(p, u, row0, vt0, vt1, seg);
         for (int vt = vt0; ok && vt < vt1; ++vt, ++lt) {
@@ -309,10 +324,10 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
             const int kk = teacher ? kb : kb - kbt;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
-              umma_bf16(d, smem_desc_sw128(sa + k * 32, 0, 1024), smem_desc_sw128(sb + k * 32, 0, 1024), kIdesc,
-                        (kk > 0 || k > 0) ? 1u : 0u);
+              umma_bf16_pair(d, smem_desc_sw128(sa + k * 32, 0, 1024), smem_desc_sw128(sb + k * 32, 0, 1024), kIdesc,
+                             (kk > 0 || k > 0) ? 1u : 0u);
             }
-            umma_commit(empty + stage);
+            umma_commit_pair(empty + stage, 0x3);
             issued = true;
             if (++stage == C::STAGES) {
               stage = 0;
@@ -320,29 +335,29 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
             }
           }
           if (!ok) break;
-          umma_commit(tfull + b);
+          umma_commit_pair(tfull + b, 0x3);
         }
       }
       if (!ok && issued) {
-        umma_commit(drain);
+        umma_commit_pair(drain, 0x1);
         drain_wait(drain, 0, 100000000ull);
       }
     }
   } else {
-    // ------------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------------ epilogue (both CTAs)
     const int e = warp - 2;         // 0..7
     const int q = warp & 3;         // TMEM lane quarter this warp may access
-    const int h = e >> 2;           // column half of the tile: [h*128, h*128+128)
-    const int row = q * 32 + lane;  // token row inside the 128-row tile
+    const int h = e >> 2;           // column half of the tile: [h*HALF, h*HALF + HALF)
+    const int row = q * 32 + lane;  // token row inside this CTA's 128 rows
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * HALF);
     float* merge = reinterpret_cast<float*>(extra);  // [kStatFields][128]
     uint8_t* staging = extra + e * 4096;             // backward: 32 rows x 128 B
     int lt = 0, lu = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x, ++lu) {
+    for (int u = cid; ok && u < p.units; u += ncl, ++lu) {
       int row0, vt0, vt1, seg;
       unit_range(p, u, row0, vt0, vt1, seg);
-      const int token = row0 + row;
+      const int token = row0 + my_rows + row;
       RowStats rs{-INFINITY, 0.f, -INFINITY, 0.f, 0.f, 0.f, false};
       float bt = 0.f, bs = 0.f;
       if (BWD && token < p.N) {
@@ -387,13 +402,13 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
               tmem_ld32(tT + c * 32, zt);
               tmem_ld32(tS + c * 32, zs);
               tmem_ld_wait();
-              const float2 c2 = make_float2(p.c, p.c), gs2 = make_float2(p.gscale, p.gscale);
+              const float2 c2v = make_float2(p.c, p.c), gs2 = make_float2(p.gscale, p.gscale);
               const float2 nbt = make_float2(-bt, -bt), nbs = make_float2(-bs, -bs), m1 = make_float2(-1.f, -1.f);
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 // p_x = exp(z_x / tau - lse_x) = 2^(z_x log2(e) / tau - lse_x log2(e))
-                const float2 pt = ex2_approx2(__ffma2_rn(make_float2(zt[2 * j], zt[2 * j + 1]), c2, nbt));
-                const float2 ps = ex2_approx2(__ffma2_rn(make_float2(zs[2 * j], zs[2 * j + 1]), c2, nbs));
+                const float2 pt = ex2_approx2(__ffma2_rn(make_float2(zt[2 * j], zt[2 * j + 1]), c2v, nbt));
+                const float2 ps = ex2_approx2(__ffma2_rn(make_float2(zs[2 * j], zs[2 * j + 1]), c2v, nbs));
                 const float2 g = __fmul2_rn(__ffma2_rn(pt, m1, ps), gs2);
                 pk[half][j] = pack_bf16x2(g.x, g.y);
               }
@@ -408,15 +423,15 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tm_G, staging, col_base + c2 * 64, row0 + q * 32);
+            if (lane == 0 && row0 + my_rows < p.N) {
+              tma_store_2d(&tm_G, staging, col_base + c2 * 64, row0 + my_rows + q * 32);
               bulk_commit_group();
             }
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty + b);
+        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + b), 0));
       }
       if (!ok) break;
       if (!BWD) {
@@ -461,9 +476,10 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no cross-CTA signal may target a CTA that has exited
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
+    tmem_dealloc_pair(tmem_base, 512);
   }
 }
 
@@ -529,33 +545,58 @@ __global__ void __launch_bounds__(1024) kl_mean_kernel(const float* __restrict__
 }
 
 template <int BN, bool BWD>
-cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(fused_kl_kernel<BN, BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              FusedCfg<BN, BWD>::SMEM);
+cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, int clusters, cudaStream_t stream) {
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = FusedCfg<BN, BWD>::SMEM;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <int BN, bool BWD>
+cudaError_t prepare_one(int* max_clusters) {
+  cudaError_t e = cudaFuncSetAttribute(fused_kl_kernel<BN, BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       FusedCfg<BN, BWD>::SMEM);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config<BN, BWD>(attr, 1, nullptr);
+  int n = 0;
+  if ((e = cudaOccupancyMaxActiveClusters(&n, fused_kl_kernel<BN, BWD>, &cfg)) != cudaSuccess) return e;
+  if (n < *max_clusters) *max_clusters = n;
+  return cudaSuccess;
 }
 
 template <int BN, bool BWD>
 cudaError_t launch_one(const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht, const CUtensorMap& Wt,
-                       const CUtensorMap& G, const FusedParams& p, int grid, cudaStream_t stream) {
-  fused_kl_kernel<BN, BWD><<<grid, kThreads, FusedCfg<BN, BWD>::SMEM, stream>>>(hs, Ws, ht, Wt, G, p);
-  return cudaGetLastError();
+                       const CUtensorMap& G, const FusedParams& p, int clusters, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config<BN, BWD>(attr, clusters, stream);
+  return cudaLaunchKernelEx(&cfg, fused_kl_kernel<BN, BWD>, hs, Ws, ht, Wt, G, p);
 }
 
 }  // namespace
 
-cudaError_t fused_prepare(int bn) {
-  if (bn != 256) return cudaErrorInvalidValue;
+cudaError_t fused_prepare(int bn, int* max_clusters) {
+  if (bn != kFusedBN) return cudaErrorInvalidValue;
+  *max_clusters = 1 << 30;
   cudaError_t e;
-  if ((e = prepare_one<256, false>()) != cudaSuccess) return e;
-  return prepare_one<256, true>();
+  if ((e = prepare_one<kFusedBN, false>(max_clusters)) != cudaSuccess) return e;
+  return prepare_one<kFusedBN, true>(max_clusters);
 }
 
 cudaError_t launch_fused(int bn, bool backward, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
-                         const CUtensorMap& Wt, const CUtensorMap& G, const FusedParams& p, int grid,
+                         const CUtensorMap& Wt, const CUtensorMap& G, const FusedParams& p, int clusters,
                          cudaStream_t stream) {
-  if (bn != 256) return cudaErrorInvalidValue;
-  return backward ? launch_one<256, true>(hs, Ws, ht, Wt, G, p, grid, stream)
-                  : launch_one<256, false>(hs, Ws, ht, Wt, G, p, grid, stream);
+  if (bn != kFusedBN) return cudaErrorInvalidValue;
+  return backward ? launch_one<kFusedBN, true>(hs, Ws, ht, Wt, G, p, clusters, stream)
+                  : launch_one<kFusedBN, false>(hs, Ws, ht, Wt, G, p, clusters, stream);
 }
 
 cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, float* kl, float* lse_s,
