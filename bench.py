@@ -40,6 +40,20 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest value over all ranks (rank 0's timing is the slowest rank's)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, steps: int, max_ms: float) -> float:
+    """Units processed by all ranks per second of the slowest rank's timed region."""
+    return units_per_rank * world * steps / (max_ms / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -282,13 +296,9 @@ def main():
     _lib.hylo_kl_sync_status(stream)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    total_ms = evs[0][0].elapsed_time(evs[-1][2])
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(evs[0][0].elapsed_time(evs[-1][2]), world, dev)
     ms_per_step = total_ms / args.steps
-    tokens_per_s = w.N * world * args.steps / (total_ms / 1e3)
+    tokens_per_s = whole_job_rate(w.N, world, args.steps, total_ms)
     tflops = w.flops_exec() * world * args.steps / (total_ms / 1e3) / 1e12
     loss_val = float(b["loss"].item())
 
@@ -326,12 +336,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e2e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": w.N * world * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": whole_job_rate(w.N, world, e2e_steps, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "api": "hylo_kl_forward + hylo_kl_backward (C ABI) with pinned-host inputs/outputs"}
         del xd, host, out_host

@@ -28,7 +28,7 @@ STATUS = {
 }
 
 EXPORTS = ("hylo_kl_workspace_bytes", "hylo_kl_forward", "hylo_kl_backward", "hylo_kl_sync_status",
-           "hylo_kl_last_error", "hylo_kl_forward_noalloc")
+           "hylo_kl_last_error", "hylo_kl_forward_noalloc", "hylo_kl_selftest_wait_timeout")
 
 
 class HyloError(RuntimeError):
@@ -57,6 +57,8 @@ def load() -> ctypes.CDLL:
     L.hylo_kl_backward.restype = ctypes.c_int
     L.hylo_kl_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, vp, vp, vp]
     L.hylo_kl_forward_noalloc.restype = ctypes.c_int
+    L.hylo_kl_selftest_wait_timeout.argtypes = [ctypes.c_int, vp]
+    L.hylo_kl_selftest_wait_timeout.restype = ctypes.c_int
     L.hylo_kl_sync_status.argtypes = [vp]
     L.hylo_kl_sync_status.restype = ctypes.c_int
     L.hylo_kl_last_error.argtypes = []
@@ -122,6 +124,10 @@ def hylo_kl_forward_noalloc(h_s, W_s, h_t, W_t, tau: float, token_chunk: int, kl
     _check(load().hylo_kl_forward_noalloc(_ptr(h_s), _ptr(W_s), _ptr(h_t), _ptr(W_t), N, d_s, d_t, V, float(tau),
                                           int(token_chunk), _ptr(kl), _ptr(lse_s), _ptr(lse_t), _ptr(loss),
                                           _stream(stream)))
+
+
+def hylo_kl_selftest_wait_timeout(limit_ms: int, stream=None) -> None:
+    _check(load().hylo_kl_selftest_wait_timeout(int(limit_ms), _stream(stream)))
 
 
 def hylo_kl_sync_status(stream=None) -> None:

@@ -16,8 +16,8 @@
 // reduce-adds (accumulate across token chunks).
 //
 // Schedule: persistent, one cluster per SM pair. The few long problem-0 tiles (K = V) are dealt
-// round-robin first; each cluster then takes a contiguous range of the short problem-1 tiles
-// sized by the host so that all clusters finish together.
+// round-robin first; the short problem-1 tiles follow round-robin in two phases (see
+// GemmParams) so that all clusters finish together and concurrent tiles share L2.
 #include "hylo_internal.h"
 
 namespace hylo {
@@ -45,23 +45,30 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsig
   }
 }
 
-// The idx-th tile of cluster `cid`: problem-0 tiles cid, cid + ncl, ..., then problem-1 tiles
-// [p1_begin[cid], p1_begin[cid + 1]).
+// The idx-th tile of cluster `cid` under the schedule described at GemmParams.
 __device__ __forceinline__ bool tile_at(const GemmParams& p, int cid, int idx, int& prob, int& t) {
-  const int t0 = p.prob[0].tiles;
-  const int n0 = t0 > cid ? (t0 - 1 - cid) / p.nclusters + 1 : 0;
+  const int ncl = p.nclusters;
+  const int t0 = p.prob[0].tiles, t1 = p.prob[1].tiles;
+  const int n0 = t0 > cid ? (t0 - 1 - cid) / ncl + 1 : 0;
   if (idx < n0) {
     prob = 0;
-    t = cid + idx * p.nclusters;
+    t = cid + idx * ncl;
     return true;
   }
-  const int j = p.p1_begin[cid] + (idx - n0);
-  if (j < p.p1_begin[cid + 1]) {
-    prob = 1;
-    t = j;
-    return true;
+  int j = idx - n0;
+  prob = 1;
+  const int rem = t0 % ncl;
+  if (rem != 0 && cid >= rem && p.p1_split > 0) {  // phase A: the clusters with one tile fewer
+    const int e = ncl - rem, k = cid - rem;
+    const int na = k < p.p1_split ? (p.p1_split - 1 - k) / e + 1 : 0;
+    if (j < na) {
+      t = k + j * e;
+      return true;
+    }
+    j -= na;
   }
-  return false;
+  t = p.p1_split + cid + j * ncl;  // phase B: all clusters
+  return t < t1;
 }
 
 // Descriptor of the k-th 16-deep slice of a staged 128-row tile.

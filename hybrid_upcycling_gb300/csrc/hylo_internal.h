@@ -47,12 +47,16 @@ struct GemmProblem {
 
 constexpr int kMaxClusters = 128;
 
-// Both gradient problems of one token chunk: problem 0 (dh_s) tiles are dealt round-robin over
-// the clusters, problem 1 (dW_s) tiles [p1_begin[c], p1_begin[c + 1]) go to cluster c.
+// Both gradient problems of one token chunk. Problem-0 (dh_s, K = V) tiles are dealt
+// round-robin over the clusters. Clusters c >= p0_rem (p0_rem = tiles0 % nclusters, when
+// nonzero) get one problem-0 tile fewer; they first share the problem-1 (dW_s) tiles
+// [0, p1_split) round-robin among themselves, then all clusters share [p1_split, tiles1)
+// round-robin, so concurrently running tiles are neighbours (their G and h_s blocks stay in L2)
+// and every cluster finishes within about one problem-1 tile of the others.
 struct GemmParams {
   GemmProblem prob[2];
   int nclusters;
-  int p1_begin[kMaxClusters + 1];
+  int p1_split;
   WaitCtl ctl;
 };
 

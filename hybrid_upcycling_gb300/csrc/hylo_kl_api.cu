@@ -166,43 +166,21 @@ int choose_segments(int64_t token_tiles, int64_t vtiles, int workers) {
   return best;
 }
 
-// Balanced static schedule of the paired gradient GEMM: problem-0 tiles (long, K = V) go
-// round-robin; each cluster then gets a count of problem-1 tiles (short) chosen so that every
-// cluster's total k-blocks reach the smallest common finish time, as contiguous ranges.
+// Phase-A size of the paired gradient GEMM schedule (see GemmParams): the clusters holding one
+// problem-0 tile fewer take that tile's worth of problem-1 tiles each before all clusters share
+// the rest.
 void schedule_gemm(GemmParams& gp) {
   const int ncl = gp.nclusters;
   const int64_t t0 = gp.prob[0].tiles, t1 = gp.prob[1].tiles;
   const int64_t k0 = gp.prob[0].kblocks, k1 = gp.prob[1].kblocks > 0 ? gp.prob[1].kblocks : 1;
-  int64_t load[kMaxClusters], w[kMaxClusters];
-  int64_t maxload = 0;
-  for (int c = 0; c < ncl; ++c) {
-    load[c] = (t0 > c ? (t0 - 1 - c) / ncl + 1 : 0) * k0;
-    if (load[c] > maxload) maxload = load[c];
+  const int64_t rem = t0 % ncl;
+  int64_t split = 0;
+  if (rem != 0) {
+    const int64_t early = ncl - rem;
+    const int64_t per = (k0 + k1 / 2) / k1;  // problem-1 tiles that fill one problem-0 tile's time
+    split = early * per;
   }
-  auto fill = [&](int64_t T) {
-    int64_t n = 0;
-    for (int c = 0; c < ncl; ++c) n += T > load[c] ? (T - load[c]) / k1 : 0;
-    return n;
-  };
-  int64_t lo = 0, hi = maxload + (t1 / ncl + 2) * k1;
-  while (lo < hi) {
-    const int64_t mid = lo + (hi - lo) / 2;
-    if (fill(mid) >= t1) hi = mid; else lo = mid + 1;
-  }
-  int64_t sum = 0;
-  for (int c = 0; c < ncl; ++c) {
-    w[c] = lo > load[c] ? (lo - load[c]) / k1 : 0;
-    sum += w[c];
-  }
-  while (sum > t1) {  // remove the excess from the clusters that would finish last
-    int cmax = -1;
-    for (int c = 0; c < ncl; ++c)
-      if (w[c] > 0 && (cmax < 0 || load[c] + w[c] * k1 > load[cmax] + w[cmax] * k1)) cmax = c;
-    --w[cmax];
-    --sum;
-  }
-  gp.p1_begin[0] = 0;
-  for (int c = 0; c < ncl; ++c) gp.p1_begin[c + 1] = gp.p1_begin[c] + static_cast<int>(w[c]);
+  gp.p1_split = static_cast<int>(split < t1 ? split : t1);
 }
 
 hylo_status check_common(const void* h_s, const void* W_s, const void* h_t, const void* W_t, int64_t N, int64_t d_s,
@@ -367,6 +345,43 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
     e = launch_gemm_pair(m_GA, m_WsB, m_dh, m_GT, m_hsB, m_dW, gp, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launch gradient GEMM");
   }
+  return HYLO_OK;
+}
+
+}  // extern "C"
+
+namespace hylo {
+namespace {
+
+// Waits on an mbarrier that nothing ever arrives on, through the same time-limited wait the
+// pipelined kernels use: the wait gives up after the limit and records a timeout in the
+// device status word, then the kernel returns normally.
+__global__ void wait_timeout_kernel(WaitCtl ctl) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_bounded(&bar, 0, &abort_flag, ctl, 99);
+}
+
+}  // namespace
+}  // namespace hylo
+
+extern "C" {
+
+hylo_status hylo_kl_selftest_wait_timeout(int limit_ms, cudaStream_t stream) {
+  g_last_error.clear();
+  if (limit_ms < 1 || limit_ms > 1000) return fail(HYLO_ERR_DIM, "limit_ms must be in [1, 1000]");
+  DeviceState* dev = nullptr;
+  hylo_status st = current_device(&dev);
+  if (st != HYLO_OK) return st;
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(WaitCtl{dev->status, static_cast<unsigned long long>(limit_ms) * 1000000ull});
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch wait-timeout self-test");
   return HYLO_OK;
 }
 

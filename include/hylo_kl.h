@@ -116,6 +116,13 @@ hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16_t* W_s,
  * (its outputs are then invalid), or HYLO_ERR_CUDA if the synchronisation failed. */
 hylo_status hylo_kl_sync_status(cudaStream_t stream);
 
+/* Diagnostic (the pages have no counterpart): enqueues on `stream` a one-warp kernel that
+ * waits on a pipeline barrier nothing ever signals, through the same time-limited wait the
+ * loss kernels use. After limit_ms (1..1000) the wait gives up, records a timeout in the device
+ * status word and the kernel returns, so the next hylo_kl_sync_status() returns
+ * HYLO_ERR_TIMEOUT and the device stays usable. Returns HYLO_ERR_DIM for other limits. */
+hylo_status hylo_kl_selftest_wait_timeout(int limit_ms, cudaStream_t stream);
+
 /* Thread-local text describing the last non-OK status returned on this thread ("" if none).
  * The pointer stays valid until the next library call on the same thread. */
 const char* hylo_kl_last_error(void);
