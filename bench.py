@@ -30,6 +30,7 @@ sys.path.insert(0, ROOT)
 from hybrid_upcycling_gb300 import synthetic as syn  # noqa: E402
 
 METRIC = "fused KL fwd+bwd tokens/s and TFLOP/s as % of GB300 dense bf16 peak"
+METRIC_LOGITS = "fused KL on logits fwd+bwd tokens/s (HBM-bound)"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
@@ -236,6 +237,97 @@ def config_dict(w):
             "l2": f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB of bf16 inputs per step; no flush)"}
 
 
+def run_logits(args, w, rank, world, local):
+    """`--path logits`: hylo_fused_kl_logits (statistics + bf16 gradient) on precomputed logits
+    of the workload's shape; one step = one call over all N rows."""
+    from hybrid_upcycling_gb300 import _lib, build
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    _lib.load()
+    z = syn.make_logits(w, device=dev)
+    f = dict(dtype=torch.float32, device=dev)
+    kl, ls, lt, loss = torch.empty(w.N, **f), torch.empty(w.N, **f), torch.empty(w.N, **f), torch.empty(1, **f)
+    dz = torch.empty(w.N, w.V, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(zz):
+        _lib.hylo_fused_kl_logits(zz["z_s"], zz["z_t"], w.tau, 1.0, kl, ls, lt, loss, dz, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step(z)
+    _lib.hylo_kl_sync_status(stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id(local)) as clk:
+        with torch.cuda.stream(stream):
+            for e in evs:
+                e[0].record(stream)
+                step(z)
+                e[1].record(stream)
+        torch.cuda.synchronize()
+    _lib.hylo_kl_sync_status(stream)
+    per = [a.elapsed_time(b) for a, b in evs]
+    total_ms = max_over_ranks(evs[0][0].elapsed_time(evs[-1][1]), world, dev)
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    alg_bytes = 6.0 * w.N * w.V  # read z_s, z_t (bf16) once, write dz_s (bf16) once
+    achieved = alg_bytes / (float(np.mean(per)) / 1e3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in z.items()}
+        for k in z:
+            host[k].copy_(z[k])
+        dz_host = torch.empty(dz.shape, dtype=dz.dtype, pin_memory=True)
+        zd = {k: torch.empty_like(v) for k, v in z.items()}
+        n_e2e = max(2, min(args.steps, 5))
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(n_e2e):
+                for k in z:
+                    zd[k].copy_(host[k], non_blocking=True)
+                step(zd)
+                dz_host.copy_(dz, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        e2e = {"value": whole_job_rate(w.N, world, n_e2e, ms), "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+               "d2h_bytes_per_step": dz_host.numel() * dz_host.element_size(), "steps": n_e2e,
+               "api": "hylo_fused_kl_logits (C ABI) with pinned-host logits and gradient"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import kl_oracle as orc
+        rows = torch.arange(0, w.N, max(1, w.N // args.cpu_tokens))[: args.cpu_tokens]
+        zs_h = z["z_s"][rows.to(dev)].double().cpu().numpy()
+        zt_h = z["z_t"][rows.to(dev)].double().cpu().numpy()
+        t0 = time.perf_counter()
+        orc.kl_from_logits(zs_h, zt_h, w.tau)
+        dt = time.perf_counter() - t0
+        cpu = {"value": len(rows) / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"{len(rows)} rows of {w.name} logits (V={w.V}), fp64 numpy, {dt:.2f} s"}
+    if rank == 0:
+        line = {
+            "metric": METRIC_LOGITS, "value": whole_job_rate(w.N, world, args.steps, total_ms), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name + "_logits", "N": w.N, "V": w.V, "tau": w.tau,
+                       "l2": f"inputs larger than L2 ({4.0 * w.N * w.V / 1e9:.2f} GB of bf16 logits per step; no flush)"},
+            "roofline": {"kernel": "kl_logits_kernel (+mean)", "bound": "hbm", "achieved": achieved, "peak": hbm,
+                         "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                         "peak_kind": f"hbm_gbs ({src})", "bytes_per_launch": alg_bytes},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -243,6 +335,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="stage2_64k", choices=list(syn.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="hidden", choices=["hidden", "logits"],
+                    help="hidden: the fused hidden-state KL (default); logits: the Fused KL on precomputed logits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample size for cpu_baseline")
@@ -262,6 +356,11 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
+    if args.path == "logits":
+        run_logits(args, w, rank, world, local)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     from hybrid_upcycling_gb300 import _lib, build
     if rank == 0:
         build.build()

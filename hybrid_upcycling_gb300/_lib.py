@@ -28,7 +28,8 @@ STATUS = {
 }
 
 EXPORTS = ("hylo_kl_workspace_bytes", "hylo_kl_forward", "hylo_kl_backward", "hylo_kl_sync_status",
-           "hylo_kl_last_error", "hylo_kl_forward_noalloc", "hylo_kl_selftest_wait_timeout")
+           "hylo_kl_last_error", "hylo_kl_forward_noalloc", "hylo_kl_selftest_wait_timeout",
+           "hylo_fused_kl_logits")
 
 
 class HyloError(RuntimeError):
@@ -57,6 +58,8 @@ def load() -> ctypes.CDLL:
     L.hylo_kl_backward.restype = ctypes.c_int
     L.hylo_kl_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, vp, vp, vp]
     L.hylo_kl_forward_noalloc.restype = ctypes.c_int
+    L.hylo_fused_kl_logits.argtypes = [vp, vp, i64, i64, i64, f32, f32, vp, vp, vp, vp, vp, vp]
+    L.hylo_fused_kl_logits.restype = ctypes.c_int
     L.hylo_kl_selftest_wait_timeout.argtypes = [ctypes.c_int, vp]
     L.hylo_kl_selftest_wait_timeout.restype = ctypes.c_int
     L.hylo_kl_sync_status.argtypes = [vp]
@@ -124,6 +127,21 @@ def hylo_kl_forward_noalloc(h_s, W_s, h_t, W_t, tau: float, token_chunk: int, kl
     _check(load().hylo_kl_forward_noalloc(_ptr(h_s), _ptr(W_s), _ptr(h_t), _ptr(W_t), N, d_s, d_t, V, float(tau),
                                           int(token_chunk), _ptr(kl), _ptr(lse_s), _ptr(lse_t), _ptr(loss),
                                           _stream(stream)))
+
+
+def hylo_fused_kl_logits(z_s, z_t, tau: float, grad_scale: float, kl, lse_s, lse_t, loss, dz_s=None,
+                         stream=None) -> None:
+    """Fused KL on bf16 logits z_s, z_t [N, V] (row stride = z.stride(0)); dz_s optional."""
+    for name, t in (("z_s", z_s), ("z_t", z_t)):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{name} must be a 2-D bfloat16 tensor with unit column stride")
+    if z_s.shape != z_t.shape or z_s.stride(0) != z_t.stride(0):
+        raise ValueError("z_s and z_t must have the same shape and row stride")
+    if dz_s is not None and (dz_s.dtype != torch.bfloat16 or dz_s.shape != z_s.shape or dz_s.stride(0) != z_s.stride(0)):
+        raise ValueError("dz_s must be bfloat16 with the shape and row stride of z_s")
+    N, V = z_s.shape
+    _check(load().hylo_fused_kl_logits(_ptr(z_s), _ptr(z_t), N, V, z_s.stride(0), float(tau), float(grad_scale),
+                                       _ptr(kl), _ptr(lse_s), _ptr(lse_t), _ptr(loss), _ptr(dz_s), _stream(stream)))
 
 
 def hylo_kl_selftest_wait_timeout(limit_ms: int, stream=None) -> None:

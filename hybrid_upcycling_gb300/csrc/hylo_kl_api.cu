@@ -385,6 +385,31 @@ hylo_status hylo_kl_selftest_wait_timeout(int limit_ms, cudaStream_t stream) {
   return HYLO_OK;
 }
 
+hylo_status hylo_fused_kl_logits(const uint16_t* z_s, const uint16_t* z_t, int64_t N, int64_t V, int64_t ld,
+                                 float tau, float grad_scale, float* kl, float* lse_s, float* lse_t, float* loss,
+                                 uint16_t* dz_s, cudaStream_t stream) {
+  g_last_error.clear();
+  if (!z_s || !z_t || !kl || !lse_s || !lse_t || !loss) return fail(HYLO_ERR_NULL, "a required pointer is NULL");
+  if (N < 1 || V < 1 || N > 0x7fffffffLL || V > 0x7fffffffLL || ld < V || ld % 8 != 0)
+    return fail(HYLO_ERR_DIM, "invalid sizes N=%lld V=%lld ld=%lld (need ld >= V, ld a multiple of 8)",
+                static_cast<long long>(N), static_cast<long long>(V), static_cast<long long>(ld));
+  if (!aligned(z_s, 16) || !aligned(z_t, 16) || (dz_s && !aligned(dz_s, 16)))
+    return fail(HYLO_ERR_ALIGN, "logit pointers must be 16-byte aligned");
+  if (!(std::isfinite(tau) && tau > 0.f)) return fail(HYLO_ERR_TAU, "tau must be finite and > 0");
+  if (!std::isfinite(grad_scale)) return fail(HYLO_ERR_TAU, "grad_scale must be finite");
+  DeviceState* dev = nullptr;
+  hylo_status st = current_device(&dev);
+  if (st != HYLO_OK) return st;
+  const float gscale = static_cast<float>(static_cast<double>(grad_scale) / (static_cast<double>(tau) * N));
+  const int grid = N < dev->sms ? static_cast<int>(N) : dev->sms;
+  cudaError_t e = launch_kl_logits(z_s, z_t, dz_s, ld, static_cast<int>(N), static_cast<int>(V), tau, gscale, kl, lse_s,
+                                   lse_t, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launch logits KL");
+  e = launch_mean(kl, static_cast<int>(N), loss, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launch mean");
+  return HYLO_OK;
+}
+
 hylo_status hylo_kl_sync_status(cudaStream_t stream) {
   g_last_error.clear();
   DeviceState* dev = nullptr;

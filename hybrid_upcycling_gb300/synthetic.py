@@ -122,6 +122,23 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None) -> Dict[s
     return out
 
 
+def make_logits(w: Workload, device="cpu", seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """Student and teacher logits [N, V] in bf16 with the spread the hidden-state workload
+    produces: independent N(0, s^2) with s^2 = w_std^2 * d (RMS-normalised hidden states; for
+    unnormalised N(0,1) hidden states the same), i.e. the logits z = h W^T would have. Near-
+    converged workloads draw z_s = z_t + N(0, (0.01 w_std)^2 d_s). Seeded like make_inputs."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed((w.seed if seed is None else seed) + 7919)
+    st = w.w_std * (w.d_t ** 0.5)
+    z_t = _randn(gen, (w.N, w.V), device) * st
+    if w.near_converged:
+        z_s = z_t + _randn(gen, (w.N, w.V), device) * (0.01 * w.w_std * (w.d_s ** 0.5))
+    else:
+        z_s = _randn(gen, (w.N, w.V), device) * (w.w_std * (w.d_s ** 0.5))
+    return {"z_s": z_s.to(torch.bfloat16), "z_t": z_t.to(torch.bfloat16)}
+
+
 def to_f64_numpy(t: torch.Tensor):
     """Widen a bf16 tensor to a float64 numpy array (exact)."""
     return t.detach().to("cpu", torch.float64).numpy()

@@ -111,6 +111,21 @@ hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16_t* W_s,
                                     float* kl, float* lse_s, float* lse_t, float* loss,
                                     cudaStream_t stream);
 
+/* "Fused KL" on precomputed logits (Long-Context Aware Upcycling digest, section Key Ideas:
+ * the memory stack lists Fused KL beside the Fused Hidden-State KL). z_s and z_t are the
+ * student's and teacher's logits, [N, V] bf16 bit patterns with row stride ld elements
+ * (ld >= V, a multiple of 8; pointers 16-byte aligned). Writes kl[N], lse_s[N], lse_t[N] and
+ * loss[0] = mean(kl) exactly as hylo_kl_forward would for logits z = h W^T, and, if dz_s is
+ * not NULL, the gradient of grad_scale * loss with respect to z_s,
+ * dz_s[n, v] = grad_scale * (p_s - p_t) / (tau N), as bf16 in an [N, ld] buffer (columns
+ * v >= V untouched). One kernel; reads each logit once for the statistics and, with a
+ * gradient, once more from L2. Needs no workspace. */
+hylo_status hylo_fused_kl_logits(const uint16_t* z_s, const uint16_t* z_t,
+                                 int64_t N, int64_t V, int64_t ld,
+                                 float tau, float grad_scale,
+                                 float* kl, float* lse_s, float* lse_t, float* loss,
+                                 uint16_t* dz_s, cudaStream_t stream);
+
 /* Synchronises `stream`, then returns and clears the current device's status word:
  * HYLO_OK, or HYLO_ERR_TIMEOUT if a kernel gave up on a pipeline wait since the last read
  * (its outputs are then invalid), or HYLO_ERR_CUDA if the synchronisation failed. */

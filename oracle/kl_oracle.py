@@ -120,3 +120,17 @@ def kl_rows(h_s, W_s, h_t, W_t, tau: float, rows: Sequence[int], grad_scale: flo
         dh[sl] = G @ W_s
     return kl, lse_s, lse_t, dh
 
+
+
+def kl_from_logits(z_s, z_t, tau: float, grad_scale: float = 1.0):
+    """The same loss on given logits ("Fused KL" of the digest's Key Ideas, applied to logits
+    that were already projected): per-token KL(p_t || p_s), both log-sum-exps, the mean loss,
+    and G = d(grad_scale * L)/dz_s = grad_scale * (p_s - p_t) / (tau N).
+    Returns (kl, lse_s, lse_t, loss, G)."""
+    N = z_s.shape[0]
+    l_s, lse_s = log_softmax(z_s, tau)
+    l_t, lse_t = log_softmax(z_t, tau)
+    p_t = np.exp(l_t)
+    kl = np.sum(p_t * (l_t - l_s), axis=1)
+    G = (np.exp(l_s) - p_t) * (grad_scale / (tau * N))
+    return kl, lse_s, lse_t, (float(np.mean(kl)) if N > 0 else 0.0), G

@@ -303,3 +303,42 @@ def test_rational_golden_fixture():
     np.testing.assert_allclose(dh, g["dh_s"], rtol=1e-11, atol=1e-16)
     np.testing.assert_allclose(dW, g["dW_s"], rtol=1e-11, atol=1e-16)
     assert all(k > 0 for k in g["kl"])
+
+
+# ----------------------------------------------------------------------------- logits input
+
+def test_logits_oracle_matches_hidden_state_oracle():
+    """On logits z = h W^T the logits-input oracle gives the pinned hidden-state results, and
+    its G contracts to the pinned gradients (dh_s = G W_s, dW_s = G^T h_s)."""
+    rng = np.random.default_rng(43)
+    h_s, W_s, h_t, W_t = _rand_problem(rng, 9, 6, 10, 37, w_std=0.5)
+    kl, ls, lt, loss = orc.kl_forward(h_s, W_s, h_t, W_t, 1.3)
+    dh, dW = orc.kl_backward(h_s, W_s, h_t, W_t, 1.3, grad_scale=0.7)
+    k2, ls2, lt2, loss2, G = orc.kl_from_logits(h_s @ W_s.T, h_t @ W_t.T, 1.3, grad_scale=0.7)
+    np.testing.assert_allclose(k2, kl, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(ls2, ls, rtol=1e-13)
+    np.testing.assert_allclose(lt2, lt, rtol=1e-13)
+    assert abs(loss2 - loss) < 1e-14
+    np.testing.assert_allclose(G @ W_s, dh, rtol=1e-11, atol=1e-16)
+    np.testing.assert_allclose(G.T @ h_s, dW, rtol=1e-11, atol=1e-16)
+
+
+def test_logits_oracle_closed_forms_and_finite_differences():
+    tau, gs = 0.9, 1.4
+    z_s = np.array([[0.3, -1.2], [2.0, 0.5], [0.0, 0.0]])
+    z_t = np.array([[1.1, 0.4], [-0.5, 0.7], [0.0, 0.0]])
+    kl, _, _, loss, G = orc.kl_from_logits(z_s, z_t, tau, gs)
+    for n in range(3):
+        p = 1.0 / (1.0 + math.exp(-(z_t[n, 1] - z_t[n, 0]) / tau))
+        q = 1.0 / (1.0 + math.exp(-(z_s[n, 1] - z_s[n, 0]) / tau))
+        ref = p * math.log(p / q) + (1 - p) * math.log((1 - p) / (1 - q))
+        assert abs(kl[n] - ref) <= 1e-12 * (1 + ref)
+    assert kl[2] == 0.0  # identical rows
+    eps = 1e-6
+    for idx in np.ndindex(*z_s.shape):
+        zp, zm = z_s.copy(), z_s.copy()
+        zp[idx] += eps
+        zm[idx] -= eps
+        fd = gs * (orc.kl_from_logits(zp, z_t, tau)[3] - orc.kl_from_logits(zm, z_t, tau)[3]) / (2 * eps)
+        assert abs(G[idx] - fd) < 1e-8
+    assert np.all(np.abs(G.sum(axis=1)) < 1e-15)  # each row of G sums to zero
