@@ -72,8 +72,10 @@ cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, fl
 cudaError_t launch_mean(const float* kl, int N, float* loss, cudaStream_t stream);
 
 // "Fused KL" on precomputed bf16 logits [N, ld] (one CTA per row at a time, `grid` CTAs).
+cudaError_t kl_logits_prepare();
 cudaError_t launch_kl_logits(const uint16_t* zs, const uint16_t* zt, uint16_t* dz, int64_t ld, int N, int V, float tau,
-                             float gscale, float* kl, float* lse_s, float* lse_t, int grid, cudaStream_t stream);
+                             float gscale, float* kl, float* lse_s, float* lse_t, const WaitCtl& ctl, int grid,
+                             cudaStream_t stream);
 
 // Paired (cta_group::2) gradient GEMM: sets the shared-memory limit and reports how many
 // 2-CTA clusters fit on the device at once; the launch runs p.nclusters clusters.

@@ -89,7 +89,7 @@ hylo_status current_device(DeviceState** out) {
       if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
       d.status = static_cast<int*>(p);
       if ((e = fused_prepare(fused_bn(), &d.fused_clusters)) != cudaSuccess ||
-          (e = gemm_prepare(&d.gemm_clusters)) != cudaSuccess)
+          (e = gemm_prepare(&d.gemm_clusters)) != cudaSuccess || (e = kl_logits_prepare()) != cudaSuccess)
         return cuda_fail(e, "kernel set-up");
       if (d.gemm_clusters < 1 || d.fused_clusters < 1)
         return fail(HYLO_ERR_CUDA, "no 2-CTA cluster of the kernels fits on the device");
@@ -403,7 +403,7 @@ hylo_status hylo_fused_kl_logits(const uint16_t* z_s, const uint16_t* z_t, int64
   const float gscale = static_cast<float>(static_cast<double>(grad_scale) / (static_cast<double>(tau) * N));
   const int grid = N < dev->sms ? static_cast<int>(N) : dev->sms;
   cudaError_t e = launch_kl_logits(z_s, z_t, dz_s, ld, static_cast<int>(N), static_cast<int>(V), tau, gscale, kl, lse_s,
-                                   lse_t, grid, stream);
+                                   lse_t, WaitCtl{dev->status, wait_limit_ns()}, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch logits KL");
   e = launch_mean(kl, static_cast<int>(N), loss, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch mean");

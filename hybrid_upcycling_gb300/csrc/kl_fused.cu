@@ -286,9 +286,9 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
             tmem_ld_wait();
             const int valid = min(32, p.V - (col_base + c * 32));
             if (valid >= 32) {
-              fold_chunk<false>(rs, zt, zs, 32, p.c, p.inv_tau);
+              fold_chunk<false>(rs, zt, zs, 0xffffffffu, p.c, p.inv_tau);
             } else if (valid > 0) {
-              fold_chunk<true>(rs, zt, zs, valid, p.c, p.inv_tau);
+              fold_chunk<true>(rs, zt, zs, (1u << valid) - 1u, p.c, p.inv_tau);
             }
           }
         } else {

@@ -40,19 +40,19 @@ __device__ __forceinline__ float2 g_series2(float2 d) {
 __device__ __forceinline__ float2 ex2_approx2(float2 x) { return make_float2(ex2_approx(x.x), ex2_approx(x.y)); }
 
 // Folds 32 columns of one row into the running statistics (column pairs in packed fp32x2
-// arithmetic). `valid` = number of columns of this chunk inside the vocabulary (32 except in
-// the last tile; MASKED only there: masked columns enter as z_t = z_s = max - 2^10 tau, whose
-// exponentials flush to zero and whose d is 0).
+// arithmetic). Column j takes part iff bit j of `valid` is set (all bits except at the end of
+// the vocabulary; MASKED only there: masked columns enter as z_t = z_s = max - 2^10 tau, whose
+// exponentials flush to zero and whose d is 0). At least one column must be valid.
 // Each column adds e_t g(d) to C: the Taylor series for |d| < 1/4, otherwise
 // e_t (exp(-d) - 1 + d) = e_s K - e_t + e_t d with K = exp((m_s - m_t)/tau), which uses no
 // extra exponential. K is clamped to stay finite; if the clamp engages the row is marked far.
 template <bool MASKED>
 __device__ __forceinline__ void fold_chunk(RowStats& r, const float (&zt_in)[32], const float (&zs_in)[32],
-                                           int valid, float c, float inv_tau) {
+                                           uint32_t valid, float c, float inv_tau) {
   float cmt = -INFINITY, cms = -INFINITY;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    if (!MASKED || j < valid) {
+    if (!MASKED || ((valid >> j) & 1u)) {
       cmt = fmaxf(cmt, zt_in[j]);
       cms = fmaxf(cms, zs_in[j]);
     }
@@ -80,8 +80,8 @@ __device__ __forceinline__ void fold_chunk(RowStats& r, const float (&zt_in)[32]
     float2 zt = make_float2(zt_in[2 * j], zt_in[2 * j + 1]);
     float2 zs = make_float2(zs_in[2 * j], zs_in[2 * j + 1]);
     if (MASKED) {
-      if (2 * j >= valid) zt.x = zs.x = fill;
-      if (2 * j + 1 >= valid) zt.y = zs.y = fill;
+      if (!((valid >> (2 * j)) & 1u)) zt.x = zs.x = fill;
+      if (!((valid >> (2 * j + 1)) & 1u)) zt.y = zs.y = fill;
     }
     const float2 et = ex2_approx2(__ffma2_rn(zt, c2, nmtc));
     const float2 es = ex2_approx2(__ffma2_rn(zs, c2, nmsc));

@@ -72,6 +72,8 @@ def logits(N, V, seed, st=1.28, ss=0.9):
     (64, 33000, 2.0, 0.5, None),     # more chunks than threads
     (1, 5, 1.0, 1.0, 8),             # tiny
     (17, 1, 1.0, 1.0, 8),            # V = 1
+    (9, 200000, 1.0, 1.0, None),     # large vocabulary, partial last chunk
+    (300, 131072, 1.0, 1.0, None),   # whole chunks only
 ])
 def test_dense_parity(N, V, tau, gs, ld):
     z_s, z_t = logits(N, V, seed=N + V)
