@@ -31,6 +31,7 @@ from hybrid_upcycling_gb300 import synthetic as syn  # noqa: E402
 
 METRIC = "fused KL fwd+bwd tokens/s and TFLOP/s as % of GB300 dense bf16 peak"
 METRIC_LOGITS = "fused KL on logits fwd+bwd tokens/s (HBM-bound)"
+METRIC_ILD = "Stage-I ILD loss fwd+bwd tokens/s (HBM-bound)"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
@@ -328,6 +329,69 @@ def run_logits(args, w, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_ild(args, rank, world, local):
+    """`--path ild`: hylo_ild_loss on the Stage-I shape of the 1B hybrid (16 layers x {layer
+    output, token-mixer output} = 32 entries, 8192 tokens = 4 x 2K sequences, d = 2048)."""
+    from hybrid_upcycling_gb300 import _lib, build
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    _lib.load()
+    P, N, d = 32, 8192, 2048
+    g = torch.Generator(device=dev)
+    g.manual_seed(1010)
+    T = torch.randn(P, N, d, generator=g, device=dev)
+    S = (T + 0.05 * torch.randn(P, N, d, generator=g, device=dev)).to(torch.bfloat16)
+    T = T.to(torch.bfloat16)
+    norms = torch.empty(P * N, device=dev)
+    loss = torch.empty(1, device=dev)
+    dS = torch.empty_like(S)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            _lib.hylo_ild_loss(S, T, 1.0, norms, loss, dS, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id(local)) as clk:
+        with torch.cuda.stream(stream):
+            for e in evs:
+                e[0].record(stream)
+                _lib.hylo_ild_loss(S, T, 1.0, norms, loss, dS, stream=stream)
+                e[1].record(stream)
+        torch.cuda.synchronize()
+    _lib.hylo_kl_sync_status(stream)
+    per = [a.elapsed_time(b) for a, b in evs]
+    total_ms = max_over_ranks(evs[0][0].elapsed_time(evs[-1][1]), world, dev)
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    alg = 6.0 * P * N * d
+    achieved = alg / (float(np.mean(per)) / 1e3) / 1e9
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import kl_oracle as orc
+        t0 = time.perf_counter()
+        orc.ild_loss(S[:, :256].double().cpu().numpy(), T[:, :256].double().cpu().numpy())
+        dt = time.perf_counter() - t0
+        cpu = {"value": 256 / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"256 tokens x {P} entries x d={d}, fp64 numpy, {dt:.2f} s"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC_ILD, "value": whole_job_rate(N, world, args.steps, total_ms), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "stage1_ild_1b", "P": P, "N": N, "d": d,
+                       "l2": f"inputs larger than L2 ({4.0 * P * N * d / 1e9:.2f} GB per step; no flush)"},
+            "roofline": {"kernel": "ild_kernel (+sum)", "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None, "peak_kind": f"hbm_gbs ({src})",
+                         "bytes_per_launch": alg},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
+        }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -335,8 +399,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="stage2_64k", choices=list(syn.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--path", default="hidden", choices=["hidden", "logits"],
-                    help="hidden: the fused hidden-state KL (default); logits: the Fused KL on precomputed logits")
+    ap.add_argument("--path", default="hidden", choices=["hidden", "logits", "ild"],
+                    help="hidden: the fused hidden-state KL (default); logits: the Fused KL on precomputed logits; "
+                         "ild: the Stage-I ILD alignment loss")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample size for cpu_baseline")
@@ -356,8 +421,11 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    if args.path == "logits":
-        run_logits(args, w, rank, world, local)
+    if args.path in ("logits", "ild"):
+        if args.path == "logits":
+            run_logits(args, w, rank, world, local)
+        else:
+            run_ild(args, rank, world, local)
         if world > 1:
             torch.distributed.destroy_process_group()
         return

@@ -29,7 +29,7 @@ STATUS = {
 
 EXPORTS = ("hylo_kl_workspace_bytes", "hylo_kl_forward", "hylo_kl_backward", "hylo_kl_sync_status",
            "hylo_kl_last_error", "hylo_kl_forward_noalloc", "hylo_kl_selftest_wait_timeout",
-           "hylo_fused_kl_logits")
+           "hylo_fused_kl_logits", "hylo_ild_loss")
 
 
 class HyloError(RuntimeError):
@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
     L.hylo_kl_forward_noalloc.restype = ctypes.c_int
     L.hylo_fused_kl_logits.argtypes = [vp, vp, i64, i64, i64, f32, f32, vp, vp, vp, vp, vp, vp]
     L.hylo_fused_kl_logits.restype = ctypes.c_int
+    L.hylo_ild_loss.argtypes = [vp, vp, i64, i64, i64, f32, vp, vp, vp, vp]
+    L.hylo_ild_loss.restype = ctypes.c_int
     L.hylo_kl_selftest_wait_timeout.argtypes = [ctypes.c_int, vp]
     L.hylo_kl_selftest_wait_timeout.restype = ctypes.c_int
     L.hylo_kl_sync_status.argtypes = [vp]
@@ -142,6 +144,19 @@ def hylo_fused_kl_logits(z_s, z_t, tau: float, grad_scale: float, kl, lse_s, lse
     N, V = z_s.shape
     _check(load().hylo_fused_kl_logits(_ptr(z_s), _ptr(z_t), N, V, z_s.stride(0), float(tau), float(grad_scale),
                                        _ptr(kl), _ptr(lse_s), _ptr(lse_t), _ptr(loss), _ptr(dz_s), _stream(stream)))
+
+
+def hylo_ild_loss(S, T, grad_scale: float, norms, loss, dS=None, stream=None) -> None:
+    """Stage-I ILD loss on stacked bf16 tensors S, T [P, N, d]; dS optional."""
+    for name, t in (("S", S), ("T", T)):
+        if t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 3-D bfloat16 tensor")
+    if S.shape != T.shape or (dS is not None and (dS.shape != S.shape or dS.dtype != torch.bfloat16
+                                                  or not dS.is_contiguous())):
+        raise ValueError("S, T (and dS) must have the same shape")
+    P, N, d = S.shape
+    _check(load().hylo_ild_loss(_ptr(S), _ptr(T), P, N, d, float(grad_scale), _ptr(norms), _ptr(loss), _ptr(dS),
+                                _stream(stream)))
 
 
 def hylo_kl_selftest_wait_timeout(limit_ms: int, stream=None) -> None:

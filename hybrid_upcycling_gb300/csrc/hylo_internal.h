@@ -77,6 +77,10 @@ cudaError_t launch_kl_logits(const uint16_t* zs, const uint16_t* zt, uint16_t* d
                              float gscale, float* kl, float* lse_s, float* lse_t, const WaitCtl& ctl, int grid,
                              cudaStream_t stream);
 
+// Stage-I Enhanced-ILD loss on stacked [P, N, d] bf16 tensors (one warp per row).
+cudaError_t launch_ild(const uint16_t* S, const uint16_t* T, int64_t P, int64_t N, int d, float grad_scale, float* norms,
+                       float* loss, uint16_t* dS, int sms, cudaStream_t stream);
+
 // Paired (cta_group::2) gradient GEMM: sets the shared-memory limit and reports how many
 // 2-CTA clusters fit on the device at once; the launch runs p.nclusters clusters.
 int gemm_smem_bytes();

@@ -410,6 +410,24 @@ hylo_status hylo_fused_kl_logits(const uint16_t* z_s, const uint16_t* z_t, int64
   return HYLO_OK;
 }
 
+hylo_status hylo_ild_loss(const uint16_t* S, const uint16_t* T, int64_t P, int64_t N, int64_t d, float grad_scale,
+                          float* norms, float* loss, uint16_t* dS, cudaStream_t stream) {
+  g_last_error.clear();
+  if (!S || !T || !norms || !loss) return fail(HYLO_ERR_NULL, "a required pointer is NULL");
+  if (P < 1 || N < 1 || d < 8 || d % 8 != 0 || d > 65536 || P * N > (int64_t(1) << 40))
+    return fail(HYLO_ERR_DIM, "invalid sizes P=%lld N=%lld d=%lld (d a multiple of 8, 8..65536)",
+                static_cast<long long>(P), static_cast<long long>(N), static_cast<long long>(d));
+  if (!aligned(S, 16) || !aligned(T, 16) || (dS && !aligned(dS, 16)))
+    return fail(HYLO_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
+  if (!std::isfinite(grad_scale)) return fail(HYLO_ERR_TAU, "grad_scale must be finite");
+  DeviceState* dev = nullptr;
+  hylo_status st = current_device(&dev);
+  if (st != HYLO_OK) return st;
+  cudaError_t e = launch_ild(S, T, P, N, static_cast<int>(d), grad_scale, norms, loss, dS, dev->sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launch ILD loss");
+  return HYLO_OK;
+}
+
 hylo_status hylo_kl_sync_status(cudaStream_t stream) {
   g_last_error.clear();
   DeviceState* dev = nullptr;

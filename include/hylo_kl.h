@@ -126,6 +126,19 @@ hylo_status hylo_fused_kl_logits(const uint16_t* z_s, const uint16_t* z_t,
                                  float* kl, float* lse_s, float* lse_t, float* loss,
                                  uint16_t* dz_s, cudaStream_t stream);
 
+/* Stage-I Enhanced-ILD alignment loss (Long-Context Aware Upcycling digest, section Method:
+ * L_ILD = sum over layers of ||h_s - h_t||_2 + ||a_s - a_t||_2, layer outputs h and token-mixer
+ * outputs a; HyLo-Llama-8MLA8GDN-8K-SFT reading notes, Stage I). S (student) and T (teacher)
+ * stack the aligned tensors as [P, N, d] bf16 bit patterns, row-major and contiguous (P = one
+ * entry per layer and per kind, N tokens, d a multiple of 8; pointers 16-byte aligned).
+ * Writes norms[p*N + n] = ||S[p,n,:] - T[p,n,:]||_2 (fp32), loss[0] = sum(norms) / N, and, if
+ * dS is not NULL, the gradient of grad_scale * loss with respect to S,
+ * grad_scale * (S - T) / (N ||S - T||) per row (0 where the row difference is 0), as bf16
+ * [P, N, d]. The teacher gets no gradient. Needs no workspace. */
+hylo_status hylo_ild_loss(const uint16_t* S, const uint16_t* T, int64_t P, int64_t N, int64_t d,
+                          float grad_scale, float* norms, float* loss, uint16_t* dS,
+                          cudaStream_t stream);
+
 /* Synchronises `stream`, then returns and clears the current device's status word:
  * HYLO_OK, or HYLO_ERR_TIMEOUT if a kernel gave up on a pipeline wait since the last read
  * (its outputs are then invalid), or HYLO_ERR_CUDA if the synchronisation failed. */

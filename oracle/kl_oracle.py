@@ -134,3 +134,24 @@ def kl_from_logits(z_s, z_t, tau: float, grad_scale: float = 1.0):
     kl = np.sum(p_t * (l_t - l_s), axis=1)
     G = (np.exp(l_s) - p_t) * (grad_scale / (tau * N))
     return kl, lse_s, lse_t, (float(np.mean(kl)) if N > 0 else 0.0), G
+
+
+def ild_loss(S, T, grad_scale: float = 1.0):
+    """Stage-I Enhanced-ILD alignment loss (Long-Context Aware Upcycling digest, section Method:
+    L_ILD = sum over layers of ||h_s - h_t||_2 + ||a_s - a_t||_2, hidden states and token-mixer
+    outputs; the reading notes' Stage I aligns each new layer with the base model's internal
+    representations). S and T stack the student and teacher tensors as [P, N, d] (P = one entry
+    per layer and per kind, h or a). Reading of the printed formula: the Euclidean norm of each
+    token's difference vector (not squared), averaged over the N tokens and summed over the P
+    entries. Returns (norms [P, N], loss, grad) with grad = grad_scale * dL/dS =
+    grad_scale * (S - T) / (N ||S - T||), taken as 0 where the difference is 0."""
+    S = np.asarray(S, dtype=np.float64)
+    T = np.asarray(T, dtype=np.float64)
+    P, N, d = S.shape
+    D = S - T
+    norms = np.sqrt(np.sum(D * D, axis=2))
+    loss = float(np.sum(norms) / N) if N > 0 else 0.0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        scale = np.where(norms > 0, grad_scale / (N * norms), 0.0)
+    grad = D * scale[:, :, None]
+    return norms, loss, grad

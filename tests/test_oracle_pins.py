@@ -342,3 +342,37 @@ def test_logits_oracle_closed_forms_and_finite_differences():
         fd = gs * (orc.kl_from_logits(zp, z_t, tau)[3] - orc.kl_from_logits(zm, z_t, tau)[3]) / (2 * eps)
         assert abs(G[idx] - fd) < 1e-8
     assert np.all(np.abs(G.sum(axis=1)) < 1e-15)  # each row of G sums to zero
+
+
+# ----------------------------------------------------------------------------- Stage-I ILD
+
+def test_ild_closed_forms():
+    """3-4-5 and 5-12-13 difference vectors have norms 5 and 13; zero differences add nothing."""
+    T = np.zeros((2, 3, 4))
+    S = np.zeros((2, 3, 4))
+    S[0, 0, :2] = [3.0, 4.0]
+    S[1, 2, 1:3] = [5.0, -12.0]
+    T[0, 1] = S[0, 1] = 7.0  # equal rows
+    norms, loss, grad = orc.ild_loss(S, T, grad_scale=2.0)
+    assert norms[0, 0] == 5.0 and norms[1, 2] == 13.0 and norms[0, 1] == 0.0
+    assert abs(loss - (5.0 + 13.0) / 3) < 1e-15
+    np.testing.assert_allclose(grad[0, 0, :2], 2.0 * np.array([3.0, 4.0]) / (3 * 5.0))
+    assert np.all(grad[0, 1] == 0.0)
+
+
+def test_ild_scaling_and_finite_differences():
+    rng = np.random.default_rng(47)
+    S = rng.standard_normal((3, 5, 6))
+    T = rng.standard_normal((3, 5, 6))
+    _, loss, grad = orc.ild_loss(S, T, grad_scale=1.5)
+    _, loss2, _ = orc.ild_loss(T + 2.5 * (S - T), T)
+    assert abs(loss2 - 2.5 * loss) < 1e-12 * loss  # norms are 1-homogeneous
+    _, loss_swapped, _ = orc.ild_loss(T, S)
+    assert abs(loss_swapped - loss) < 1e-13 * loss  # symmetric in student and teacher
+    eps = 1e-6
+    for idx in [(0, 0, 0), (1, 3, 2), (2, 4, 5), (0, 2, 3)]:
+        Sp, Sm = S.copy(), S.copy()
+        Sp[idx] += eps
+        Sm[idx] -= eps
+        fd = 1.5 * (orc.ild_loss(Sp, T)[1] - orc.ild_loss(Sm, T)[1]) / (2 * eps)
+        assert abs(grad[idx] - fd) < 1e-8
