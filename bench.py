@@ -111,6 +111,7 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # let nvidia-smi start sampling before the timed region begins
         except Exception:
             self.proc = None
         return self
@@ -162,6 +163,7 @@ def make_buffers(w, x, dev):
         "ws": torch.empty(_lib.hylo_kl_workspace_bytes(w.N, w.d_s, w.d_t, w.V, w.token_chunk), dtype=torch.uint8,
                           device=dev),
         "kl": torch.empty(w.N, **f), "lse_s": torch.empty(w.N, **f), "lse_t": torch.empty(w.N, **f),
+        "gap": torch.empty(w.N, **f),
         "loss": torch.empty(1, **f), "dh": torch.empty(w.N, w.d_s, **f), "dW": torch.empty(w.V, w.d_s, **f),
     }
     return b
@@ -172,11 +174,11 @@ def step(w, x, b, stream, ev=None):
     if ev is not None:
         ev[0].record(stream)
     _lib.hylo_kl_forward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, w.token_chunk, b["kl"], b["lse_s"],
-                         b["lse_t"], b["loss"], b["ws"], stream=stream)
+                         b["lse_t"], b["loss"], b["ws"], stream=stream, lse_gap=b["gap"])
     if ev is not None:
         ev[1].record(stream)
     _lib.hylo_kl_backward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, w.token_chunk, b["lse_s"], b["lse_t"], 1.0,
-                          b["dh"], b["dW"], b["ws"], stream=stream)
+                          b["dh"], b["dW"], b["ws"], stream=stream, lse_gap=b["gap"])
     if ev is not None:
         ev[2].record(stream)
 
@@ -184,6 +186,17 @@ def step(w, x, b, stream, ev=None):
 def launches_per_step(w) -> int:
     chunks = math.ceil(w.N / min(w.token_chunk, w.N))
     return 3 + 2 * chunks  # fused fwd + combine + mean; per chunk: fused G + paired dh/dW GEMM
+
+
+def time_repeated(fn, min_s: float = 10.0, max_calls: int = 10000):
+    """Calls fn() until at least min_s seconds have passed; returns (calls, seconds)."""
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        calls += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_s or calls >= max_calls:
+            return calls, dt
 
 
 def cpu_oracle_rate(w, x, sample_tokens: int, repeats: int = 1):
@@ -204,31 +217,82 @@ def cpu_oracle_rate(w, x, sample_tokens: int, repeats: int = 1):
 
 
 def run_reference(args, w, rank, world):
-    """Reference arm: the fp64 CPU oracle on the host cores (rank 0 only)."""
+    """Reference arm: the fp64 CPU oracle on the host cores (rank 0 only), on the same path,
+    workload and metric as our arm, each step a sample of `--ref-tokens` tokens."""
     if rank != 0:
         return
+    from oracle import kl_oracle as orc
     torch.manual_seed(0)
-    x = syn.make_inputs(w, device="cuda" if torch.cuda.is_available() else "cpu")
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
     tokens = args.ref_tokens
+    if args.path == "hidden":
+        x = syn.make_inputs(w, device=dev)
+        one = lambda: cpu_oracle_rate(w, x, tokens)[1]
+        metric, config = METRIC, config_dict(w)
+        sample = f"{tokens} tokens of {w.name} per step (full V={w.V}, d_s={w.d_s}, d_t={w.d_t}), fp64 numpy"
+    elif args.path == "logits":
+        z = syn.make_logits(w, device=dev)
+        rows = torch.arange(tokens) * max(1, w.N // tokens)
+        zs_h = z["z_s"][rows.to(z["z_s"].device)].double().cpu().numpy()
+        zt_h = z["z_t"][rows.to(z["z_t"].device)].double().cpu().numpy()
+        del z
+
+        def one():
+            t0 = time.perf_counter()
+            orc.kl_from_logits(zs_h, zt_h, w.tau)
+            return time.perf_counter() - t0
+        metric, config = METRIC_LOGITS, config_logits(w)
+        sample = f"{tokens} rows of {w.name} logits per step (V={w.V}), fp64 numpy"
+    else:
+        S, T = ild_states(dev)
+        Sh, Th = S[:, :tokens].double().cpu().numpy(), T[:, :tokens].double().cpu().numpy()
+        del S, T
+
+        def one():
+            t0 = time.perf_counter()
+            orc.ild_loss(Sh, Th)
+            return time.perf_counter() - t0
+        metric, config = METRIC_ILD, config_ild()
+        sample = f"{tokens} tokens x {ILD_SHAPE[0]} entries x d={ILD_SHAPE[2]} per step, fp64 numpy"
     for _ in range(args.warmup):
-        cpu_oracle_rate(w, x, tokens)
-    times = []
-    for _ in range(args.steps):
-        _, dt = cpu_oracle_rate(w, x, tokens)
-        times.append(dt)
+        one()
+    times = [one() for _ in range(args.steps)]
     tot = sum(times)
     value = tokens * args.steps / tot
     cores = len(os.sched_getaffinity(0))
-    sample = f"{tokens} tokens of {w.name} per step (full V={w.V}, d_s={w.d_s}, d_t={w.d_t}), fp64 numpy"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w),
+        "config": config,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+ILD_SHAPE = (32, 8192, 2048)  # 16 layers x {layer output, token-mixer output}, 4 x 2K tokens, d = 2048
+
+
+def ild_states(dev):
+    """Seeded Stage-I states: teacher N(0, 1), student = teacher + 0.05 N(0, 1), both bf16."""
+    P, N, d = ILD_SHAPE
+    g = torch.Generator(device=dev)
+    g.manual_seed(1010)
+    T = torch.randn(P, N, d, generator=g, device=dev)
+    S = (T + 0.05 * torch.randn(P, N, d, generator=g, device=dev)).to(torch.bfloat16)
+    return S, T.to(torch.bfloat16)
+
+
+def config_logits(w):
+    return {"workload": w.name + "_logits", "N": w.N, "V": w.V, "tau": w.tau,
+            "l2": f"inputs larger than L2 ({4.0 * w.N * w.V / 1e9:.2f} GB of bf16 logits per step; no flush)"}
+
+
+def config_ild():
+    P, N, d = ILD_SHAPE
+    return {"workload": "stage1_ild_1b", "P": P, "N": N, "d": d,
+            "l2": f"inputs larger than L2 ({4.0 * P * N * d / 1e9:.2f} GB per step; no flush)"}
 
 
 def config_dict(w):
@@ -309,18 +373,16 @@ def run_logits(args, w, rank, world, local):
         rows = torch.arange(0, w.N, max(1, w.N // args.cpu_tokens))[: args.cpu_tokens]
         zs_h = z["z_s"][rows.to(dev)].double().cpu().numpy()
         zt_h = z["z_t"][rows.to(dev)].double().cpu().numpy()
-        t0 = time.perf_counter()
-        orc.kl_from_logits(zs_h, zt_h, w.tau)
-        dt = time.perf_counter() - t0
-        cpu = {"value": len(rows) / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-               "sample": f"{len(rows)} rows of {w.name} logits (V={w.V}), fp64 numpy, {dt:.2f} s"}
+        calls, dt = time_repeated(lambda: orc.kl_from_logits(zs_h, zt_h, w.tau))
+        cpu = {"value": calls * len(rows) / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+               "kind": "oracle",
+               "sample": f"{calls} x {len(rows)} rows of {w.name} logits (V={w.V}), fp64 numpy, {dt:.1f} s"}
     if rank == 0:
         line = {
             "metric": METRIC_LOGITS, "value": whole_job_rate(w.N, world, args.steps, total_ms), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name + "_logits", "N": w.N, "V": w.V, "tau": w.tau,
-                       "l2": f"inputs larger than L2 ({4.0 * w.N * w.V / 1e9:.2f} GB of bf16 logits per step; no flush)"},
+            "config": config_logits(w),
             "roofline": {"kernel": "kl_logits_kernel (+mean)", "bound": "hbm", "achieved": achieved, "peak": hbm,
                          "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
                          "peak_kind": f"hbm_gbs ({src})", "bytes_per_launch": alg_bytes},
@@ -339,12 +401,8 @@ def run_ild(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     _lib.load()
-    P, N, d = 32, 8192, 2048
-    g = torch.Generator(device=dev)
-    g.manual_seed(1010)
-    T = torch.randn(P, N, d, generator=g, device=dev)
-    S = (T + 0.05 * torch.randn(P, N, d, generator=g, device=dev)).to(torch.bfloat16)
-    T = T.to(torch.bfloat16)
+    P, N, d = ILD_SHAPE
+    S, T = ild_states(dev)
     norms = torch.empty(P * N, device=dev)
     loss = torch.empty(1, device=dev)
     dS = torch.empty_like(S)
@@ -370,32 +428,60 @@ def run_ild(args, rank, world, local):
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     alg = 6.0 * P * N * d
     achieved = alg / (float(np.mean(per)) / 1e3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        S_h = torch.empty(S.shape, dtype=S.dtype, pin_memory=True)
+        T_h = torch.empty(T.shape, dtype=T.dtype, pin_memory=True)
+        S_h.copy_(S)
+        T_h.copy_(T)
+        dS_h = torch.empty(dS.shape, dtype=dS.dtype, pin_memory=True)
+        loss_h = torch.empty(1, pin_memory=True)
+        Sd, Td = torch.empty_like(S), torch.empty_like(T)
+        n_e2e = 5
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(n_e2e):
+                Sd.copy_(S_h, non_blocking=True)
+                Td.copy_(T_h, non_blocking=True)
+                _lib.hylo_ild_loss(Sd, Td, 1.0, norms, loss, dS, stream=stream)
+                dS_h.copy_(dS, non_blocking=True)
+                loss_h.copy_(loss, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        e2e = {"value": whole_job_rate(N, world, n_e2e, ms), "unit": "tokens/s",
+               "h2d_bytes_per_step": 2 * S.numel() * S.element_size(),
+               "d2h_bytes_per_step": dS.numel() * dS.element_size() + 4, "steps": n_e2e,
+               "api": "hylo_ild_loss (C ABI) with pinned-host states, gradient and loss"}
+        del Sd, Td, S_h, T_h, dS_h
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import kl_oracle as orc
-        t0 = time.perf_counter()
-        orc.ild_loss(S[:, :256].double().cpu().numpy(), T[:, :256].double().cpu().numpy())
-        dt = time.perf_counter() - t0
-        cpu = {"value": 256 / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-               "sample": f"256 tokens x {P} entries x d={d}, fp64 numpy, {dt:.2f} s"}
+        Sh, Th = S[:, :256].double().cpu().numpy(), T[:, :256].double().cpu().numpy()
+        calls, dt = time_repeated(lambda: orc.ild_loss(Sh, Th))
+        cpu = {"value": 256 * calls / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"{calls} x 256 tokens x {P} entries x d={d}, fp64 numpy, {dt:.1f} s"}
     if rank == 0:
         print(json.dumps({
             "metric": METRIC_ILD, "value": whole_job_rate(N, world, args.steps, total_ms), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "stage1_ild_1b", "P": P, "N": N, "d": d,
-                       "l2": f"inputs larger than L2 ({4.0 * P * N * d / 1e9:.2f} GB per step; no flush)"},
+            "config": config_ild(),
             "roofline": {"kernel": "ild_kernel (+sum)", "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": None, "peak_kind": f"hbm_gbs ({src})",
                          "bytes_per_launch": alg},
-            "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
         }), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 10; 300 for --path logits and 500 for --path ild, whose steps "
+                         "take about a millisecond, so that the clock sampler sees the timed region)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="stage2_64k", choices=list(syn.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -407,6 +493,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample size for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=48, help="oracle tokens per reference-arm step")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 10 if args.impl == "reference" else {"hidden": 10, "logits": 300, "ild": 500}[args.path]
     rank, world, local = dist_env()
     w = syn.WORKLOADS[args.workload]
 
@@ -511,10 +599,12 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, dt = cpu_oracle_rate(w, x, args.cpu_tokens)
+        res = []
+        calls, dt = time_repeated(lambda: res.append(cpu_oracle_rate(w, x, args.cpu_tokens)[1]))
+        rate = args.cpu_tokens * calls / sum(res)
         cpu = {"value": rate, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-               "sample": f"{args.cpu_tokens} tokens of {w.name} (full V and d), fp64 numpy forward+backward, "
-                         f"{dt:.1f} s"}
+               "sample": f"{calls} x {args.cpu_tokens} tokens of {w.name} (full V and d), fp64 numpy "
+                         f"forward+backward, {sum(res):.1f} s"}
 
     if rank == 0:
         line = {

@@ -52,11 +52,11 @@ def load() -> ctypes.CDLL:
     i64, f32, vp, sz = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
     L.hylo_kl_workspace_bytes.argtypes = [i64, i64, i64, i64, i64]
     L.hylo_kl_workspace_bytes.restype = sz
-    L.hylo_kl_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, vp, vp, vp, sz, vp]
+    L.hylo_kl_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, vp, vp, vp, vp, sz, vp]
     L.hylo_kl_forward.restype = ctypes.c_int
-    L.hylo_kl_backward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, f32, vp, vp, vp, sz, vp]
+    L.hylo_kl_backward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, vp, f32, vp, vp, vp, sz, vp]
     L.hylo_kl_backward.restype = ctypes.c_int
-    L.hylo_kl_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, vp, vp, vp]
+    L.hylo_kl_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, vp, vp, vp, vp]
     L.hylo_kl_forward_noalloc.restype = ctypes.c_int
     L.hylo_fused_kl_logits.argtypes = [vp, vp, i64, i64, i64, f32, f32, vp, vp, vp, vp, vp, vp]
     L.hylo_fused_kl_logits.restype = ctypes.c_int
@@ -106,29 +106,31 @@ def hylo_kl_workspace_bytes(N: int, d_s: int, d_t: int, V: int, token_chunk: int
 
 
 def hylo_kl_forward(h_s, W_s, h_t, W_t, tau: float, token_chunk: int, kl, lse_s, lse_t, loss, workspace,
-                    stream=None) -> None:
+                    stream=None, lse_gap=None) -> None:
+    """lse_gap (optional fp32 [N]) receives the precise lse_s - lse_t for hylo_kl_backward."""
     N, d_s, d_t, V = _dims(h_s, W_s, h_t, W_t)
     _check(load().hylo_kl_forward(_ptr(h_s), _ptr(W_s), _ptr(h_t), _ptr(W_t), N, d_s, d_t, V, float(tau),
-                                  int(token_chunk), _ptr(kl), _ptr(lse_s), _ptr(lse_t), _ptr(loss),
+                                  int(token_chunk), _ptr(kl), _ptr(lse_s), _ptr(lse_t), _ptr(lse_gap), _ptr(loss),
                                   _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def hylo_kl_backward(h_s, W_s, h_t, W_t, tau: float, token_chunk: int, lse_s, lse_t, grad_scale: float, dh_s,
-                     dW_s, workspace, stream=None) -> None:
+                     dW_s, workspace, stream=None, lse_gap=None) -> None:
+    """lse_gap (optional) is the forward's precise lse_s - lse_t; None uses lse_s - lse_t."""
     N, d_s, d_t, V = _dims(h_s, W_s, h_t, W_t)
     _check(load().hylo_kl_backward(_ptr(h_s), _ptr(W_s), _ptr(h_t), _ptr(W_t), N, d_s, d_t, V, float(tau),
-                                   int(token_chunk), _ptr(lse_s), _ptr(lse_t), float(grad_scale), _ptr(dh_s),
-                                   _ptr(dW_s), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   int(token_chunk), _ptr(lse_s), _ptr(lse_t), _ptr(lse_gap), float(grad_scale),
+                                   _ptr(dh_s), _ptr(dW_s), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)))
 
 
 def hylo_kl_forward_noalloc(h_s, W_s, h_t, W_t, tau: float, token_chunk: int, kl, lse_s, lse_t, loss,
-                            stream=None) -> None:
+                            stream=None, lse_gap=None) -> None:
     """hylo_kl_forward without a workspace: the library's built-in scratch is used instead."""
     N, d_s, d_t, V = _dims(h_s, W_s, h_t, W_t)
     _check(load().hylo_kl_forward_noalloc(_ptr(h_s), _ptr(W_s), _ptr(h_t), _ptr(W_t), N, d_s, d_t, V, float(tau),
-                                          int(token_chunk), _ptr(kl), _ptr(lse_s), _ptr(lse_t), _ptr(loss),
-                                          _stream(stream)))
+                                          int(token_chunk), _ptr(kl), _ptr(lse_s), _ptr(lse_t), _ptr(lse_gap),
+                                          _ptr(loss), _stream(stream)))
 
 
 def hylo_fused_kl_logits(z_s, z_t, tau: float, grad_scale: float, kl, lse_s, lse_t, loss, dz_s=None,

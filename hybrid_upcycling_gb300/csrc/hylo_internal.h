@@ -31,6 +31,7 @@ struct FusedParams {
   float* part;      // forward: partial statistics [kStatFields][nseg][N]
   const float* lse_s;  // backward: per-token log-sum-exps (natural log of sum exp(z/tau))
   const float* lse_t;
+  const float* lse_gap;  // backward: precise lse_s - lse_t per token, or null (then lse_s - lse_t)
   float gscale;     // backward: grad_scale / (tau * N_total)
   WaitCtl ctl;
 };
@@ -68,13 +69,14 @@ cudaError_t launch_fused(int bn, bool backward, const CUtensorMap& hs, const CUt
                          const CUtensorMap& Wt, const CUtensorMap& G, const FusedParams& p, int clusters,
                          cudaStream_t stream);
 cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, float* kl, float* lse_s,
-                           float* lse_t, cudaStream_t stream);
+                           float* lse_t, float* lse_gap, cudaStream_t stream);
 cudaError_t launch_mean(const float* kl, int N, float* loss, cudaStream_t stream);
 
-// "Fused KL" on precomputed bf16 logits [N, ld] (one CTA per row at a time, `grid` CTAs).
-cudaError_t kl_logits_prepare();
+// "Fused KL" on precomputed bf16 logits [N, ld]: one row per cluster at a time (clusters of
+// kSplit CTAs). kl_logits_prepare reports how many clusters fit on the device at once.
+cudaError_t kl_logits_prepare(int* max_clusters);
 cudaError_t launch_kl_logits(const uint16_t* zs, const uint16_t* zt, uint16_t* dz, int64_t ld, int N, int V, float tau,
-                             float gscale, float* kl, float* lse_s, float* lse_t, const WaitCtl& ctl, int grid,
+                             float gscale, float* kl, float* lse_s, float* lse_t, const WaitCtl& ctl, int clusters,
                              cudaStream_t stream);
 
 // Stage-I Enhanced-ILD loss on stacked [P, N, d] bf16 tensors (one warp per row).

@@ -29,6 +29,7 @@ struct DeviceState {
   int sms = 0;
   int gemm_clusters = 0;   // 2-CTA clusters of the gradient GEMM resident at once
   int fused_clusters = 0;  // 2-CTA clusters of the fused kernels resident at once
+  int logits_clusters = 0; // clusters of the logits kernel resident at once
   int* status = nullptr;
   std::string why;
 };
@@ -89,10 +90,10 @@ hylo_status current_device(DeviceState** out) {
       if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
       d.status = static_cast<int*>(p);
       if ((e = fused_prepare(fused_bn(), &d.fused_clusters)) != cudaSuccess ||
-          (e = gemm_prepare(&d.gemm_clusters)) != cudaSuccess || (e = kl_logits_prepare()) != cudaSuccess)
+          (e = gemm_prepare(&d.gemm_clusters)) != cudaSuccess || (e = kl_logits_prepare(&d.logits_clusters)) != cudaSuccess)
         return cuda_fail(e, "kernel set-up");
-      if (d.gemm_clusters < 1 || d.fused_clusters < 1)
-        return fail(HYLO_ERR_CUDA, "no 2-CTA cluster of the kernels fits on the device");
+      if (d.gemm_clusters < 1 || d.fused_clusters < 1 || d.logits_clusters < 1)
+        return fail(HYLO_ERR_CUDA, "no thread-block cluster of the kernels fits on the device");
       if (d.gemm_clusters > kMaxClusters) d.gemm_clusters = kMaxClusters;
       if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
@@ -216,7 +217,7 @@ size_t hylo_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V, i
 
 hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t, const uint16_t* W_t,
                             int64_t N, int64_t d_s, int64_t d_t, int64_t V, float tau, int64_t token_chunk,
-                            float* kl, float* lse_s, float* lse_t, float* loss, void* workspace,
+                            float* kl, float* lse_s, float* lse_t, float* lse_gap, float* loss, void* workspace,
                             size_t workspace_bytes, cudaStream_t stream) {
   g_last_error.clear();
   (void)token_chunk;  // the forward needs O(N) scratch whatever the chunk
@@ -251,7 +252,7 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
 
   cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
-  e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, stream);
+  e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, lse_gap, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch combine");
   e = launch_mean(kl, p.N, loss, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch mean");
@@ -260,7 +261,8 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
 
 hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t, const uint16_t* W_t,
                              int64_t N, int64_t d_s, int64_t d_t, int64_t V, float tau, int64_t token_chunk,
-                             const float* lse_s, const float* lse_t, float grad_scale, float* dh_s, float* dW_s,
+                             const float* lse_s, const float* lse_t, const float* lse_gap, float grad_scale,
+                             float* dh_s, float* dW_s,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   g_last_error.clear();
   if (!lse_s || !lse_t || !dh_s || !dW_s) return fail(HYLO_ERR_NULL, "an lse or gradient pointer is NULL");
@@ -313,6 +315,7 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
     p.inv_tau = 1.0f / tau;
     p.lse_s = lse_s + c0;
     p.lse_t = lse_t + c0;
+    p.lse_gap = lse_gap != nullptr ? lse_gap + c0 : nullptr;
     p.gscale = gscale;
     p.ctl = ctl;
     const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
@@ -401,9 +404,9 @@ hylo_status hylo_fused_kl_logits(const uint16_t* z_s, const uint16_t* z_t, int64
   hylo_status st = current_device(&dev);
   if (st != HYLO_OK) return st;
   const float gscale = static_cast<float>(static_cast<double>(grad_scale) / (static_cast<double>(tau) * N));
-  const int grid = N < dev->sms ? static_cast<int>(N) : dev->sms;
+  const int clusters = N < dev->logits_clusters ? static_cast<int>(N) : dev->logits_clusters;
   cudaError_t e = launch_kl_logits(z_s, z_t, dz_s, ld, static_cast<int>(N), static_cast<int>(V), tau, gscale, kl, lse_s,
-                                   lse_t, WaitCtl{dev->status, wait_limit_ns()}, grid, stream);
+                                   lse_t, WaitCtl{dev->status, wait_limit_ns()}, clusters, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch logits KL");
   e = launch_mean(kl, static_cast<int>(N), loss, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch mean");
@@ -492,7 +495,7 @@ hylo_status noalloc_scratch(float** out) {
 extern "C" hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t,
                                                const uint16_t* W_t, int64_t N, int64_t d_s, int64_t d_t, int64_t V,
                                                float tau, int64_t token_chunk, float* kl, float* lse_s,
-                                               float* lse_t, float* loss, cudaStream_t stream) {
+                                               float* lse_t, float* lse_gap, float* loss, cudaStream_t stream) {
   g_last_error.clear();
   (void)token_chunk;
   if (!h_s || !W_s || !h_t || !W_t || !kl || !lse_s || !lse_t || !loss)
@@ -540,7 +543,7 @@ extern "C" hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16
 
   cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
-  e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, stream);
+  e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, lse_gap, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch combine");
   e = launch_mean(kl, p.N, loss, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch mean");

@@ -260,10 +260,12 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
       unit_range(p, u, row0, vt0, vt1, seg);
       const int token = row0 + my_rows + row;
       RowStats rs{-INFINITY, 0.f, -INFINITY, 0.f, 0.f, 0.f, false};
-      float bt = 0.f, bs = 0.f;
+      float bt = 0.f, bs = 0.f, ngl = 0.f;
       if (BWD && token < p.N) {
-        bt = p.lse_t[token] * kLog2e;
-        bs = p.lse_s[token] * kLog2e;
+        const float lt_ = p.lse_t[token], ls_ = p.lse_s[token];
+        bt = lt_ * kLog2e;
+        bs = ls_ * kLog2e;
+        ngl = -(p.lse_gap != nullptr ? p.lse_gap[token] : ls_ - lt_) * kLog2e;
       }
       for (int vt = vt0; vt < vt1; ++vt, ++lt) {
         const int b = lt % NBUF;
@@ -304,13 +306,12 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
               tmem_ld32(tS + c * 32, zs);
               tmem_ld_wait();
               const float2 c2v = make_float2(p.c, p.c), gs2 = make_float2(p.gscale, p.gscale);
-              const float2 nbt = make_float2(-bt, -bt), nbs = make_float2(-bs, -bs), m1 = make_float2(-1.f, -1.f);
+              const float2 nbt = make_float2(-bt, -bt), nbs = make_float2(-bs, -bs), ngl2 = make_float2(ngl, ngl);
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                // p_x = exp(z_x / tau - lse_x) = 2^(z_x log2(e) / tau - lse_x log2(e))
-                const float2 pt = ex2_approx2(__ffma2_rn(make_float2(zt[2 * j], zt[2 * j + 1]), c2v, nbt));
-                const float2 ps = ex2_approx2(__ffma2_rn(make_float2(zs[2 * j], zs[2 * j + 1]), c2v, nbs));
-                const float2 g = __fmul2_rn(__ffma2_rn(pt, m1, ps), gs2);
+                const float2 g = __fmul2_rn(prob_diff2(make_float2(zt[2 * j], zt[2 * j + 1]),
+                                                       make_float2(zs[2 * j], zs[2 * j + 1]), c2v, nbt, nbs, ngl2),
+                                            gs2);
                 pk[half][j] = pack_bf16x2(g.x, g.y);
               }
             }
@@ -384,13 +385,15 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
   }
 }
 
-// Merges the per-segment statistics of each token (fp64) and writes kl, lse_s, lse_t.
+// Merges the per-segment statistics of each token (fp64) and writes kl, lse_s, lse_t and,
+// when `gap` is not null, the precise lse_s - lse_t.
 // KL = A/S_t - lse_t + lse_s in general; when C is valid (marked by C >= 0) and the two
 // distributions are close, the algebraically equal form
 // KL = C' + log1p(C' - mu) - (C' - mu), with mu = A/S_t = E_pt[d] and
 // C' = C/S_t = E_pt[exp(-d) - 1 + d] >= 0, avoids the cancellation of two ~log V terms.
 __global__ void kl_combine_kernel(const float* __restrict__ part, int N, int nseg, float inv_tau,
-                                  float* __restrict__ kl, float* __restrict__ lse_s, float* __restrict__ lse_t) {
+                                  float* __restrict__ kl, float* __restrict__ lse_s, float* __restrict__ lse_t,
+                                  float* __restrict__ gap) {
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= N) return;
   const size_t NS = static_cast<size_t>(N);
@@ -415,11 +418,12 @@ __global__ void kl_combine_kernel(const float* __restrict__ part, int N, int nse
     Cc += wt * cs;
     Ss += ws * b[3 * fs + s * NS];
   }
-  double lt, ls;
-  const double k = kl_from_stats(Mt, St, Ms, Ss, A, Cc, far, it, lt, ls);
+  double lt, ls, gp;
+  const double k = kl_from_stats(Mt, St, Ms, Ss, A, Cc, far, it, lt, ls, gp);
   kl[n] = static_cast<float>(k);
   lse_s[n] = static_cast<float>(ls);
   lse_t[n] = static_cast<float>(lt);
+  if (gap != nullptr) gap[n] = static_cast<float>(gp);
 }
 
 // loss[0] = mean(kl[0..N)) with a fixed-order fp64 reduction (one block).
@@ -492,9 +496,10 @@ cudaError_t launch_fused(int bn, bool backward, const CUtensorMap& hs, const CUt
 }
 
 cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, float* kl, float* lse_s,
-                           float* lse_t, cudaStream_t stream) {
+                           float* lse_t, float* gap, cudaStream_t stream) {
   const int threads = 256;
-  kl_combine_kernel<<<(N + threads - 1) / threads, threads, 0, stream>>>(part, N, nseg, inv_tau, kl, lse_s, lse_t);
+  kl_combine_kernel<<<(N + threads - 1) / threads, threads, 0, stream>>>(part, N, nseg, inv_tau, kl, lse_s, lse_t,
+                                                                         gap);
   return cudaGetLastError();
 }
 

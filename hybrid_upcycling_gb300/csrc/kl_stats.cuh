@@ -119,16 +119,42 @@ __device__ __forceinline__ void merge_stats(RowStats& r, const RowStats& o, floa
 // exp(max/tau)): lse_x = m_x/tau + log S_x and KL = A/S_t - lse_t + lse_s; when C is valid
 // (not `far`) and the two distributions are close (|C' - mu| < 1/2, mu = A/S_t, C' = C/S_t),
 // the algebraically equal KL = C' + log1p(C' - mu) - (C' - mu) avoids subtracting two ~log V
-// numbers.
+// numbers. The same quantity gives the gap lse_s - lse_t = log1p(C' - mu) (C' - mu =
+// sum_v e_t (exp(-d_v) - 1) / S_t = S_s exp((m_s - m_t)/tau) / S_t - 1), exact to a few fp32
+// ulps of the gap itself rather than of lse.
 __device__ __forceinline__ double kl_from_stats(double mt, double st, double ms, double ss, double a, double cc,
-                                                bool far, double inv_tau, double& lse_t, double& lse_s) {
+                                                bool far, double inv_tau, double& lse_t, double& lse_s,
+                                                double& gap) {
   lse_t = mt * inv_tau + log(st);
   lse_s = ms * inv_tau + log(ss);
   const double mu = a / st;
   const double cn = cc / st;
   const double u = cn - mu;
-  if (!far && isfinite(u) && fabs(u) < 0.5) return cn + (log1p(u) - u);
+  if (!far && isfinite(u) && fabs(u) < 0.5) {
+    gap = log1p(u);
+    return cn + (log1p(u) - u);
+  }
+  gap = lse_s - lse_t;
   return mu - lse_t + lse_s;
+}
+
+// (p_s - p_t) for two columns, p_x = 2^(z_x c - b_x) with c = log2(e)/tau, b_x = lse_x log2(e).
+// Where the two probabilities are close, |D| < 1/64 with D = (z_s - z_t) c - (lse_s - lse_t)
+// log2(e) = log2(p_s / p_t), the difference is formed as p_t (2^D - 1), 2^D - 1 = e^x - 1 by
+// its Taylor series x + x^2/2 + x^3/6 in x = D ln 2 (truncation < 6e-8 relative there), so
+// that near-identical distributions lose no digits to cancellation; elsewhere |p_s - p_t| is
+// at least 1% of p_t and the direct p_s - p_t keeps ~1e-4 relative accuracy, far below the
+// bf16 rounding of the result. `ngl` is -(lse_s - lse_t) log2(e) from the precise gap.
+__device__ __forceinline__ float2 prob_diff2(float2 zt, float2 zs, float2 c2, float2 nbt, float2 nbs, float2 ngl) {
+  const float2 pt = ex2_approx2(__ffma2_rn(zt, c2, nbt));
+  const float2 ps = ex2_approx2(__ffma2_rn(zs, c2, nbs));
+  const float2 D = __ffma2_rn(__fadd2_rn(zs, make_float2(-zt.x, -zt.y)), c2, ngl);
+  const float2 x = __fmul2_rn(D, make_float2(0.6931471805599453f, 0.6931471805599453f));
+  float2 t = __ffma2_rn(x, make_float2(1.0f / 6.0f, 1.0f / 6.0f), make_float2(0.5f, 0.5f));
+  t = __ffma2_rn(x, t, make_float2(1.0f, 1.0f));
+  const float2 small = __fmul2_rn(pt, __fmul2_rn(x, t));
+  const float2 big = __fadd2_rn(ps, make_float2(-pt.x, -pt.y));
+  return make_float2(fabsf(D.x) < 0.015625f ? small.x : big.x, fabsf(D.y) < 0.015625f ? small.y : big.y);
 }
 
 }  // namespace hylo

@@ -79,6 +79,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return done != 0;
 }
 
+// The same with cluster-scope acquire: shared-memory stores that other CTAs of the cluster made
+// into this CTA before their release-arrive on `bar` are visible once it succeeds.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done) : "r"(bar_addr), "r"(parity), "n"(kSuspendHintNs) : "memory");
+  return done != 0;
+}
+
 // Controls shared by every role of a pipelined kernel.
 struct WaitCtl {
   int* status;                 // device status word (first error code wins)
@@ -91,13 +103,16 @@ enum : int { kDevTimeoutBase = 0x1000 };
 // Waits until the phase with parity `parity` of `bar` has completed. Returns false if the
 // CTA's abort flag is raised or the time limit passes (then it raises the flag itself and
 // records kDevTimeoutBase + site in the status word).
+// kClusterAcquire: wait with cluster-scope acquire (see mbar_try_wait_cluster).
+template <bool kClusterAcquire = false>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                              const WaitCtl& ctl, int site) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  auto probe = [&]() { return kClusterAcquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
+  if (probe()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (probe()) return true;
     if ((it & 3u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > ctl.limit_ns) {
@@ -230,6 +245,10 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(cluster_addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {

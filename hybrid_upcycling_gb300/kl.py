@@ -14,7 +14,7 @@ from . import _lib
 
 def _alloc_outputs(N: int, device):
     f = dict(dtype=torch.float32, device=device)
-    return torch.empty(N, **f), torch.empty(N, **f), torch.empty(N, **f), torch.empty(1, **f)
+    return torch.empty(N, **f), torch.empty(N, **f), torch.empty(N, **f), torch.empty(N, **f), torch.empty(1, **f)
 
 
 def workspace(N: int, d_s: int, d_t: int, V: int, token_chunk: int, device) -> torch.Tensor:
@@ -30,23 +30,24 @@ class FusedHiddenStateKL(torch.autograd.Function):
         N, d_s = h_s.shape
         V, d_t = W_t.shape
         ws = workspace(N, d_s, d_t, V, token_chunk, h_s.device)
-        kl, lse_s, lse_t, loss = _alloc_outputs(N, h_s.device)
-        _lib.hylo_kl_forward(h_s, W_s, h_t, W_t, tau, token_chunk, kl, lse_s, lse_t, loss, ws)
-        ctx.save_for_backward(h_s, W_s, h_t, W_t, lse_s, lse_t)
+        kl, lse_s, lse_t, gap, loss = _alloc_outputs(N, h_s.device)
+        _lib.hylo_kl_forward(h_s, W_s, h_t, W_t, tau, token_chunk, kl, lse_s, lse_t, loss, ws, lse_gap=gap)
+        ctx.save_for_backward(h_s, W_s, h_t, W_t, lse_s, lse_t, gap)
         ctx.tau, ctx.token_chunk = tau, token_chunk
         ctx.mark_non_differentiable(kl)
         return loss[0], kl
 
     @staticmethod
     def backward(ctx, g_loss, g_kl):
-        h_s, W_s, h_t, W_t, lse_s, lse_t = ctx.saved_tensors
+        h_s, W_s, h_t, W_t, lse_s, lse_t, gap = ctx.saved_tensors
         N, d_s = h_s.shape
         V, d_t = W_t.shape
         ws = workspace(N, d_s, d_t, V, ctx.token_chunk, h_s.device)
         dh_s = torch.empty(N, d_s, dtype=torch.float32, device=h_s.device)
         dW_s = torch.empty(V, d_s, dtype=torch.float32, device=h_s.device)
         scale = 1.0 if g_loss is None else float(g_loss)  # one host read of the upstream scalar
-        _lib.hylo_kl_backward(h_s, W_s, h_t, W_t, ctx.tau, ctx.token_chunk, lse_s, lse_t, scale, dh_s, dW_s, ws)
+        _lib.hylo_kl_backward(h_s, W_s, h_t, W_t, ctx.tau, ctx.token_chunk, lse_s, lse_t, scale, dh_s, dW_s, ws,
+                              lse_gap=gap)
         return dh_s.to(h_s.dtype), dW_s.to(W_s.dtype), None, None, None, None
 
 

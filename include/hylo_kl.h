@@ -67,26 +67,34 @@ size_t hylo_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
 /* Forward: kl[N], lse_s[N], lse_t[N] (natural-log units of z/tau) and loss[0] = mean(kl).
  * One fused pass: each CTA computes student and teacher logit tiles on the tensor cores and
  * folds them into running softmax/KL statistics; nothing of size N x V is written.
+ * lse_gap[N] is optional (NULL: not written): lse_s - lse_t computed from the statistics as
+ * log1p of a sum of per-word differences, so it keeps the digits that the difference of the
+ * two fp32 lse values (each rounded at ~1e-6 of log V) loses when the distributions are
+ * close; hand it to hylo_kl_backward.
  * token_chunk (<= 0 means 4096) does not change the results; the forward uses O(N) scratch
- * whatever its value. kl, lse_s, lse_t and loss may not alias the inputs. */
+ * whatever its value. kl, lse_s, lse_t, lse_gap and loss may not alias the inputs. */
 hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s,
                             const uint16_t* h_t, const uint16_t* W_t,
                             int64_t N, int64_t d_s, int64_t d_t, int64_t V,
                             float tau, int64_t token_chunk,
-                            float* kl, float* lse_s, float* lse_t, float* loss,
+                            float* kl, float* lse_s, float* lse_t, float* lse_gap, float* loss,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Backward: dh_s [N, d_s] and dW_s [V, d_s] (fp32, OVERWRITTEN, not accumulated) for
- * grad_scale * loss, from the lse_s / lse_t that hylo_kl_forward wrote for the same inputs.
- * Per token chunk it recomputes both logit tiles, forms G in bf16 in the workspace
- * (token_chunk x V), then runs dh_s = G W_s and dW_s += G^T h_s on the tensor cores.
- * Results match for any token_chunk up to fp32 summation order. */
+ * grad_scale * loss, from the lse_s / lse_t (and lse_gap, if not NULL) that hylo_kl_forward
+ * wrote for the same inputs. Per token chunk it recomputes both logit tiles, forms G in bf16
+ * in the workspace (token_chunk x V), then runs dh_s = G W_s and dW_s += G^T h_s on the
+ * tensor cores. Where p_s and p_t of a word agree to within a factor 2^(1/4), G takes the form
+ * p_t (2^D - 1), D = log2(p_s / p_t) from the logit difference and lse_gap, which has no
+ * cancellation; with lse_gap NULL the gap is lse_s - lse_t, whose rounding bounds the
+ * relative accuracy of G at ~1e-6 / |p_s / p_t - 1|. Results match for any token_chunk up
+ * to fp32 summation order. */
 hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s,
                              const uint16_t* h_t, const uint16_t* W_t,
                              int64_t N, int64_t d_s, int64_t d_t, int64_t V,
                              float tau, int64_t token_chunk,
-                             const float* lse_s, const float* lse_t, float grad_scale,
-                             float* dh_s, float* dW_s,
+                             const float* lse_s, const float* lse_t, const float* lse_gap,
+                             float grad_scale, float* dh_s, float* dW_s,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Forward that allocates nothing and takes no workspace. (The pages describe no such call;
@@ -108,8 +116,8 @@ hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16_t* W_s,
                                     const uint16_t* h_t, const uint16_t* W_t,
                                     int64_t N, int64_t d_s, int64_t d_t, int64_t V,
                                     float tau, int64_t token_chunk,
-                                    float* kl, float* lse_s, float* lse_t, float* loss,
-                                    cudaStream_t stream);
+                                    float* kl, float* lse_s, float* lse_t, float* lse_gap,
+                                    float* loss, cudaStream_t stream);
 
 /* "Fused KL" on precomputed logits (Long-Context Aware Upcycling digest, section Key Ideas:
  * the memory stack lists Fused KL beside the Fused Hidden-State KL). z_s and z_t are the

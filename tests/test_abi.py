@@ -59,20 +59,20 @@ FAKE = 0x10000  # a 256-byte aligned non-null address; never dereferenced by the
 
 def _fwd(lib, **kw):
     a = dict(h_s=FAKE, W_s=FAKE, h_t=FAKE, W_t=FAKE, N=16, d_s=64, d_t=128, V=100, tau=1.0, chunk=4096,
-             kl=FAKE, lse_s=FAKE, lse_t=FAKE, loss=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
+             kl=FAKE, lse_s=FAKE, lse_t=FAKE, gap=None, loss=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
     a.update(kw)
     return lib.hylo_kl_forward(a["h_s"], a["W_s"], a["h_t"], a["W_t"], a["N"], a["d_s"], a["d_t"], a["V"],
-                               a["tau"], a["chunk"], a["kl"], a["lse_s"], a["lse_t"], a["loss"], a["ws"],
+                               a["tau"], a["chunk"], a["kl"], a["lse_s"], a["lse_t"], a["gap"], a["loss"], a["ws"],
                                a["wsb"], a["stream"])
 
 
 def _bwd(lib, **kw):
     a = dict(h_s=FAKE, W_s=FAKE, h_t=FAKE, W_t=FAKE, N=16, d_s=64, d_t=128, V=100, tau=1.0, chunk=4096,
-             lse_s=FAKE, lse_t=FAKE, gs=1.0, dh=FAKE, dW=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
+             lse_s=FAKE, lse_t=FAKE, gap=None, gs=1.0, dh=FAKE, dW=FAKE, ws=FAKE, wsb=1 << 30, stream=None)
     a.update(kw)
     return lib.hylo_kl_backward(a["h_s"], a["W_s"], a["h_t"], a["W_t"], a["N"], a["d_s"], a["d_t"], a["V"],
-                                a["tau"], a["chunk"], a["lse_s"], a["lse_t"], a["gs"], a["dh"], a["dW"], a["ws"],
-                                a["wsb"], a["stream"])
+                                a["tau"], a["chunk"], a["lse_s"], a["lse_t"], a["gap"], a["gs"], a["dh"], a["dW"],
+                                a["ws"], a["wsb"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,status", [

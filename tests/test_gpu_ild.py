@@ -44,8 +44,11 @@ def states(P, N, d, seed, rel=0.2):
 
 
 @pytest.mark.parametrize("P,N,d,gs", [(4, 37, 2048, 1.0), (3, 5, 8, 0.5), (2, 129, 2056, 2.0), (1, 1, 24, 1.0),
-                                      (32, 256, 4096, 1.0)])
+                                      (32, 256, 4096, 1.0), (2, 33, 6144, 1.0), (1, 17, 16384, 0.7),
+                                      (1, 5, 20000, 1.0), (3, 41, 1000, 1.0)])
 def test_dense_parity(P, N, d, gs):
+    # d spans one warp per row (<= 2048), groups of 2, 4 and 8 warps (<= 16384) and the
+    # re-reading one-warp kernel for longer rows; 1000 leaves a ragged last vector group
     S, T = states(P, N, d, seed=P * N + d)
     norms, loss, dS = run(S, T, gs)
     rn, rl, rg = orc.ild_loss(f64(S), f64(T), gs)

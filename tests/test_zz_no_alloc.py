@@ -16,7 +16,7 @@ FAKE = 0x10000
 
 
 def _noalloc(lib, N=16, d_s=64, d_t=128, V=100, ptr=FAKE, tau=1.0):
-    return lib.hylo_kl_forward_noalloc(ptr, ptr, ptr, ptr, N, d_s, d_t, V, tau, 4096, ptr, ptr, ptr, ptr, None)
+    return lib.hylo_kl_forward_noalloc(ptr, ptr, ptr, ptr, N, d_s, d_t, V, tau, 4096, ptr, ptr, ptr, None, ptr, None)
 
 
 def test_noalloc_rejects_bad_arguments_without_touching_the_gpu():
