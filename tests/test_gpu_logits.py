@@ -1,8 +1,8 @@
 """GPU parity of the logits-input "Fused KL" (hylo_fused_kl_logits) against the fp64 oracle.
 
 Tolerances: per token |dkl| <= 1e-3 (1 + kl), mean loss 1e-4 relative, lse 2e-5 (1 + |lse|) as
-for the hidden-state path; dz_s is stored in bf16, whose rounding alone is at most 2^-9 of each
-element, so ||d dz_s||_F <= 2e-3 ||dz_s||_F.
+for the hidden-state path; dz_s is stored in bf16, whose rounding alone is at most 2^-8 of each
+element and ~1.7e-3 rms over many elements, so ||d dz_s||_F <= 2e-3 ||dz_s||_F.
 """
 import numpy as np
 import pytest
