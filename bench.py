@@ -67,19 +67,27 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+# Per path: the committed DRAM-traffic record of its dominant kernel (profiles/) and the
+# sources of that kernel's translation unit; a record stays valid while they are unchanged.
+TRAFFIC_RECORDS = {
+    "hidden": ("fused_fwd_traffic.txt", ("kl_fused.cu", "kl_stats.cuh", "sm103_ptx.cuh", "hylo_internal.h")),
+    "logits": ("kl_logits_traffic.txt", ("kl_logits.cu", "kl_stats.cuh", "sm103_ptx.cuh", "hylo_internal.h")),
+    "ild": ("ild_traffic.txt", ("ild.cu", "sm103_ptx.cuh", "hylo_internal.h")),
+}
+
+
+def kernel_source_hash(path: str = "hidden") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "hybrid_upcycling_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+    for fn in TRAFFIC_RECORDS[path][1]:
+        h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the fused forward kernel from the committed ncu summary, if it
-    was taken from the current kernel sources (else None)."""
-    p = os.path.join(ROOT, "profiles", "fused_fwd_traffic.txt")
+def recorded_traffic(workload: str, path: str = "hidden"):
+    """DRAM bytes per launch of the path's dominant kernel from the committed ncu summary, if
+    it was taken from the current kernel sources and for this workload (else None)."""
+    p = os.path.join(ROOT, "profiles", TRAFFIC_RECORDS[path][0])
     if not os.path.exists(p):
         return None
     kv = {}
@@ -87,7 +95,7 @@ def recorded_traffic(workload: str):
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("source_hash") != kernel_source_hash() or kv.get("workload") != workload:
+    if kv.get("source_hash") != kernel_source_hash(path) or kv.get("workload") != workload:
         return None
     try:
         return float(kv["dram_bytes_per_launch"])
@@ -384,7 +392,8 @@ def run_logits(args, w, rank, world, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_logits(w),
             "roofline": {"kernel": "kl_logits_kernel (+mean)", "bound": "hbm", "achieved": achieved, "peak": hbm,
-                         "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                         "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": recorded_traffic(config_logits(w)["workload"], "logits"),
                          "peak_kind": f"hbm_gbs ({src})", "bytes_per_launch": alg_bytes},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
         }
@@ -469,9 +478,9 @@ def run_ild(args, rank, world, local):
             "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_ild(),
-            "roofline": {"kernel": "ild_kernel (+sum)", "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": None, "peak_kind": f"hbm_gbs ({src})",
-                         "bytes_per_launch": alg},
+            "roofline": {"kernel": "ild_reg_kernel (+sum)", "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": recorded_traffic(config_ild()["workload"], "ild"),
+                         "peak_kind": f"hbm_gbs ({src})", "bytes_per_launch": alg},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
         }), flush=True)
 

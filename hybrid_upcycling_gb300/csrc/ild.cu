@@ -152,13 +152,21 @@ __global__ void __launch_bounds__(kThreads) ild_kernel(const uint16_t* __restric
   }
 }
 
-// loss[0] = sum(norms[0..rows)) / N, fixed-order fp64 reduction (one block).
+// loss[0] = sum(norms[0..rows)) / N in a fixed order (one block): each thread sums its strided
+// share in fp32 with Kahan compensation (error ~2 ulp whatever the count; GB300's fp64 rate is
+// too low for hundreds of thousands of fp64 adds on one SM), then the 1024 partials are added
+// in fp64 by a fixed tree.
 __global__ void __launch_bounds__(1024) ild_sum_kernel(const float* __restrict__ norms, int64_t rows, int64_t N,
                                                        float* loss) {
   __shared__ double red[1024];
-  double s = 0;
-  for (int64_t i = threadIdx.x; i < rows; i += 1024) s += static_cast<double>(norms[i]);
-  red[threadIdx.x] = s;
+  float s = 0.f, comp = 0.f;
+  for (int64_t i = threadIdx.x; i < rows; i += 1024) {
+    const float y = norms[i] - comp;
+    const float t = s + y;
+    comp = (t - s) - y;
+    s = t;
+  }
+  red[threadIdx.x] = static_cast<double>(s) - static_cast<double>(comp);
   __syncthreads();
   for (int w = 512; w > 0; w >>= 1) {
     if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
