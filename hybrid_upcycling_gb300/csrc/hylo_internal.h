@@ -25,6 +25,7 @@ struct FusedParams {
   int token_tiles;  // ceil(N / 256): 256-token pair tiles
   int vtiles;       // ceil(V / kFusedBN)
   int nseg;         // vocabulary segments per pair tile
+  int group;        // pair tiles per raster group (see unit_range)
   int units;        // token_tiles * nseg
   float c;          // log2(e) / tau
   float inv_tau;    // 1 / tau

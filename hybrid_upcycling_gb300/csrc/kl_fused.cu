@@ -71,8 +71,18 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsig
 
 // Work unit u = (256-token pair tile, vocabulary segment); row0 = the pair tile's first token.
 __device__ __forceinline__ void unit_range(const FusedParams& p, int u, int& row0, int& vt0, int& vt1, int& seg) {
-  const int ti = u / p.nseg;
-  seg = u - ti * p.nseg;
+  // Grouped raster: units run group by group (p.group pair tiles x every segment), segment-major
+  // inside a group. The clusters active at any time then share few segments, each swept in the
+  // same order by many clusters (its LM-head tiles come from DRAM about once and from L2 for the
+  // others), while the group's hidden-state tiles, re-read for every vocabulary tile, stay
+  // within an L2-sized working set.
+  const int per_group = p.group * p.nseg;
+  const int g = u / per_group;
+  const int t0 = g * p.group;
+  const int gt = min(p.group, p.token_tiles - t0);  // pair tiles in this group (the last may be short)
+  const int r = u - g * per_group;
+  seg = r / gt;
+  const int ti = t0 + (r - seg * gt);
   row0 = ti * 2 * kBM;
   vt0 = static_cast<int>((static_cast<long long>(seg) * p.vtiles) / p.nseg);
   vt1 = static_cast<int>((static_cast<long long>(seg + 1) * p.vtiles) / p.nseg);
