@@ -575,36 +575,58 @@ def main():
     # ----------------------------------------------------------------- end-to-end via host buffers
     e2e = None
     if not args.no_e2e:
+        # Every step copies its inputs in from pinned host memory and its results (kl, loss, dh_s,
+        # dW_s) out, double-buffered: the copies of step k+1's inputs and of step k-1's results
+        # run on their own streams while step k computes.
         host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in x.items()}
         for k in x:
             host[k].copy_(x[k])
-        xd = {k: torch.empty_like(v) for k, v in x.items()}
-        out_host = {k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True) for k in ("kl", "loss", "dh", "dW")}
+        outs = ("kl", "loss", "dh", "dW")
+        xd = [{k: torch.empty_like(v) for k, v in x.items()} for _ in range(2)]
+        bo = [b, {k: (v if k == "ws" else torch.empty_like(v)) for k, v in b.items()}]
+        out_host = [{k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True) for k in outs} for _ in range(2)]
         h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+        d2h = sum(v.numel() * v.element_size() for v in out_host[0].values())
         e2e_steps = max(2, min(args.steps, 5))
-        with torch.cuda.stream(stream):
+        cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(cin):
             for k in x:  # warm the copy path once
-                xd[k].copy_(host[k], non_blocking=True)
+                xd[0][k].copy_(host[k], non_blocking=True)
         torch.cuda.synchronize()
         barrier()
+        ev = lambda: torch.cuda.Event(enable_timing=False)
+        ev_in, ev_comp, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(e2e_steps):
+        e0.record(cin)
+        for i in range(e2e_steps):
+            s = i % 2
+            with torch.cuda.stream(cin):
+                if i >= 2:
+                    cin.wait_event(ev_comp[s])  # step i-2 has finished reading slot s
                 for k in x:
-                    xd[k].copy_(host[k], non_blocking=True)
-                step(w, xd, b, stream)
-                for k in out_host:
-                    out_host[k].copy_(b[k], non_blocking=True)
-        e1.record(stream)
+                    xd[s][k].copy_(host[k], non_blocking=True)
+                ev_in[s].record(cin)
+            stream.wait_event(ev_in[s])
+            if i >= 2:
+                stream.wait_event(ev_out[s])  # step i-2's results have left slot s
+            with torch.cuda.stream(stream):
+                step(w, xd[s], bo[s], stream)
+                ev_comp[s].record(stream)
+            with torch.cuda.stream(cout):
+                cout.wait_event(ev_comp[s])
+                for k in outs:
+                    out_host[s][k].copy_(bo[s][k], non_blocking=True)
+                ev_out[s].record(cout)
+        e1.record(cout)
         torch.cuda.synchronize()
         barrier()
+        _lib.hylo_kl_sync_status(stream)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         e2e = {"value": whole_job_rate(w.N, world, e2e_steps, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-               "api": "hylo_kl_forward + hylo_kl_backward (C ABI) with pinned-host inputs/outputs"}
-        del xd, host, out_host
+               "api": "hylo_kl_forward + hylo_kl_backward (C ABI) with pinned-host inputs/outputs, "
+                      "copies double-buffered on their own streams"}
+        del xd, host, out_host, bo
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
