@@ -15,12 +15,12 @@
 // next-token distributions, kl_weight 1.0, no cross-entropy (HyLo-Llama-8MLA8GDN-8K-SFT reading
 // notes, kwkr.cn, section "two-stage training recipe", Stage II).
 //
-// Roles (384 threads, three warpgroups): warp 0 issues TMA loads, warp 1 owns TMEM and issues
-// the UMMAs, warps 2..3 idle; warps 4..11 are the epilogue. Warp w reads TMEM lanes
-// 32*(w%4) .. 32*(w%4)+31, so each epilogue thread owns one token row of the 128-row tile;
-// warps 4..7 take columns 0..127 of the 256-column tile and warps 8..11 columns 128..255. Each epilogue thread first copies its 128
-// teacher logits into registers and releases the teacher accumulator, so the next tile's
-// teacher UMMAs run while the epilogue works on the student half.
+// Roles (320 threads per CTA): warp 0 issues the TMA loads, warp 1 of the even CTA owns TMEM
+// and issues the UMMAs for the pair, warps 2..9 are the epilogue. Warp w may read only TMEM
+// lanes 32*(w%4) .. 32*(w%4)+31, so each epilogue thread owns one token row of its CTA's
+// 128-row tile: warps 2..5 take columns 0..127 of the 256-column tile, warps 6..9 columns
+// 128..255 (lane quarter w & 3, column half (w - 2) >> 2). The (teacher, student) accumulator
+// pair fills TMEM and is drained between tiles.
 #include <cfloat>
 #include <cmath>
 
