@@ -433,7 +433,7 @@ hylo_status hylo_ild_loss(const uint16_t* S, const uint16_t* T, int64_t P, int64
                           float* norms, float* loss, uint16_t* dS, cudaStream_t stream) {
   g_last_error.clear();
   if (!S || !T || !norms || !loss) return fail(HYLO_ERR_NULL, "a required pointer is NULL");
-  if (P < 1 || N < 1 || d < 8 || d % 8 != 0 || d > 65536 || P * N > (int64_t(1) << 40))
+  if (P < 1 || N < 1 || d < 8 || d % 8 != 0 || d > 65536 || N > (int64_t(1) << 40) / P)
     return fail(HYLO_ERR_DIM, "invalid sizes P=%lld N=%lld d=%lld (d a multiple of 8, 8..65536)",
                 static_cast<long long>(P), static_cast<long long>(N), static_cast<long long>(d));
   if (!aligned(S, 16) || !aligned(T, 16) || (dS && !aligned(dS, 16)))

@@ -101,3 +101,38 @@ def test_valid_call_without_gpu_fails_cleanly(lib):
     st = _fwd(lib)
     assert st in (-6, -8)
     assert lib.hylo_kl_last_error()
+
+
+def _logits(lib, **kw):
+    a = dict(zs=FAKE, zt=FAKE, N=16, V=100, ld=104, tau=1.0, gs=1.0, kl=FAKE, ls=FAKE, lt=FAKE, loss=FAKE, dz=FAKE,
+             stream=None)
+    a.update(kw)
+    return lib.hylo_fused_kl_logits(a["zs"], a["zt"], a["N"], a["V"], a["ld"], a["tau"], a["gs"], a["kl"], a["ls"],
+                                    a["lt"], a["loss"], a["dz"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(zs=None), -1), (dict(loss=None), -1), (dict(N=0), -2), (dict(V=0), -2), (dict(ld=99), -2),
+    (dict(ld=100), -2), (dict(zt=FAKE + 2), -3), (dict(dz=FAKE + 8), -3), (dict(tau=0.0), -4),
+    (dict(gs=float("nan")), -4),
+])
+def test_logits_rejects_bad_arguments(lib, kw, status):
+    assert _logits(lib, **kw) == status
+    assert lib.hylo_kl_last_error()
+
+
+def _ild(lib, **kw):
+    a = dict(S=FAKE, T=FAKE, P=4, N=16, d=64, gs=1.0, norms=FAKE, loss=FAKE, dS=FAKE, stream=None)
+    a.update(kw)
+    return lib.hylo_ild_loss(a["S"], a["T"], a["P"], a["N"], a["d"], a["gs"], a["norms"], a["loss"], a["dS"],
+                             a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(S=None), -1), (dict(norms=None), -1), (dict(P=0), -2), (dict(N=-1), -2), (dict(d=4), -2),
+    (dict(d=68), -2), (dict(d=65544), -2), (dict(P=1 << 30, N=1 << 30), -2), (dict(T=FAKE + 4), -3),
+    (dict(dS=FAKE + 2), -3), (dict(gs=float("inf")), -4),
+])
+def test_ild_rejects_bad_arguments(lib, kw, status):
+    assert _ild(lib, **kw) == status
+    assert lib.hylo_kl_last_error()
