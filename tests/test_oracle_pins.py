@@ -376,3 +376,47 @@ def test_ild_scaling_and_finite_differences():
         Sm[idx] -= eps
         fd = 1.5 * (orc.ild_loss(Sp, T)[1] - orc.ild_loss(Sm, T)[1]) / (2 * eps)
         assert abs(grad[idx] - fd) < 1e-8
+
+
+# ------------------------------------------------- the algebra the kernels use, in fp64
+
+@pytest.mark.parametrize("shift,noise", [(0.0, 1.0), (0.0, 1e-3), (3.0, 1e-2)])
+def test_online_statistics_forms_match_the_definition(shift, noise):
+    """The kernels never form the softmaxes: they keep, per token, running maxima m_x, sums
+    S_x = sum exp((z_x - m_x)/tau), A = sum e_t d and C = sum e_t (exp(-d) - 1 + d) with
+    d = (z_t - z_s)/tau, e_t = exp((z_t - m_t)/tau), merged chunk by chunk with rescaling, and
+    read off lse_x = m_x/tau + log S_x, KL = A/S_t - lse_t + lse_s, the cancellation-free
+    KL = C' + log1p(u) - u and the gap lse_s - lse_t = log1p(u) (u = C' - A/S_t, C' = C/S_t).
+    Here, in fp64 and independently of the oracle's code path, each form against the oracle's
+    definition, including a common shift of the student logits (KL unchanged, gap moves)."""
+    rng = np.random.default_rng(97)
+    tau, V, chunk = 1.3, 1000, 96
+    z_t = rng.standard_normal((5, V)) * 1.5
+    z_s = z_t + shift + noise * rng.standard_normal((5, V))
+    kl, ls, lt, _, _ = orc.kl_from_logits(z_s, z_t, tau)
+    for n in range(5):
+        mt = ms = -np.inf
+        st = ss = a = c = 0.0
+        for c0 in range(0, V, chunk):  # online fold, ragged last chunk
+            zt, zs = z_t[n, c0:c0 + chunk], z_s[n, c0:c0 + chunk]
+            nmt, nms = max(mt, zt.max()), max(ms, zs.max())
+            wt, ws = math.exp((mt - nmt) / tau), math.exp((ms - nms) / tau)
+            st, a, c, ss = st * wt, a * wt, c * wt, ss * ws
+            mt, ms = nmt, nms
+            et, es = np.exp((zt - mt) / tau), np.exp((zs - ms) / tau)
+            d = (zt - zs) / tau
+            st += et.sum()
+            ss += es.sum()
+            a += (et * d).sum()
+            c += (et * (np.exp(-d) - 1 + d)).sum()
+        lse_t, lse_s = mt / tau + math.log(st), ms / tau + math.log(ss)
+        mu, cn = a / st, c / st
+        u = cn - mu
+        assert abs(lse_t - lt[n]) < 1e-12 * (1 + abs(lt[n]))
+        assert abs(lse_s - ls[n]) < 1e-12 * (1 + abs(ls[n]))
+        assert abs((mu - lse_t + lse_s) - kl[n]) < 1e-11 * (1 + abs(lse_t))
+        if abs(u) < 0.5:  # the regime the kernels take this form in: no cancellation
+            assert abs((cn + math.log1p(u) - u) - kl[n]) < 1e-12 * kl[n] + 1e-18
+        else:  # still exact algebra, but cn and u are large next to KL here
+            assert abs((cn + math.log1p(u) - u) - kl[n]) < 1e-13 * (1 + cn + abs(u))
+        assert abs(math.log1p(u) - (ls[n] - lt[n])) < 1e-12 * (1 + abs(ls[n]))
