@@ -415,8 +415,9 @@ def test_online_statistics_forms_match_the_definition(shift, noise):
         assert abs(lse_t - lt[n]) < 1e-12 * (1 + abs(lt[n]))
         assert abs(lse_s - ls[n]) < 1e-12 * (1 + abs(ls[n]))
         assert abs((mu - lse_t + lse_s) - kl[n]) < 1e-11 * (1 + abs(lse_t))
-        if abs(u) < 0.5:  # the regime the kernels take this form in: no cancellation
-            assert abs((cn + math.log1p(u) - u) - kl[n]) < 1e-12 * kl[n] + 1e-18
+        if abs(u) < 0.5:  # the regime the kernels take this form in: no cancellation (the
+            # oracle's own sum of p_t (l_t - l_s) keeps ~1e-10 of a KL this small)
+            assert abs((cn + (math.log1p(u) - u)) - kl[n]) < 1e-9 * kl[n] + 1e-18
         else:  # still exact algebra, but cn and u are large next to KL here
             assert abs((cn + math.log1p(u) - u) - kl[n]) < 1e-13 * (1 + cn + abs(u))
         assert abs(math.log1p(u) - (ls[n] - lt[n])) < 1e-12 * (1 + abs(ls[n]))
