@@ -651,6 +651,8 @@ def main():
                          "flops_per_launch": w.flops_fwd()},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step(w) * args.steps,
             "clocks": clk.summary(),
+            "memory": {"workspace_bytes": int(b["ws"].numel()), "dense_fp32_logits_bytes": 4 * w.N * w.V,
+                       "note": "the library allocates nothing; the caller's workspace is its only scratch"},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -251,6 +251,35 @@ def test_runs_on_a_side_stream():
         assert torch.equal(ref[k], got[k]), k
 
 
+def test_library_allocates_no_device_memory():
+    """The caller owns every byte: after a first call on the device (one-time set-up), a
+    forward + backward leaves the device's free memory unchanged, so the peak extra memory is
+    the workspace the caller passed -- O(N + token_chunk V), not the O(N V) of dense logits."""
+    N, d_s, d_t, V, chunk = 1000, 128, 256, 5000, 512
+    x = gen(N, d_s, d_t, V, seed=12)
+    ws = torch.empty(_lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, chunk), dtype=torch.uint8, device="cuda")
+    f = dict(dtype=torch.float32, device="cuda")
+    kl, ls, lt, gap = (torch.empty(N, **f) for _ in range(4))
+    loss = torch.empty(1, **f)
+    dh, dW = torch.empty(N, d_s, **f), torch.empty(V, d_s, **f)
+
+    def call():
+        _lib.hylo_kl_forward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], 1.0, chunk, kl, ls, lt, loss, ws, lse_gap=gap)
+        _lib.hylo_kl_backward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], 1.0, chunk, ls, lt, 1.0, dh, dW, ws, lse_gap=gap)
+        _lib.hylo_kl_sync_status()
+
+    call()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    call()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    # O(N) statistics or one chunk's bf16 G, whichever is larger; below one model's fp32 logits
+    assert ws.numel() <= max(6 * 32 * N * 4, chunk * ((V + 7) // 8 * 8) * 2) + 256
+    assert ws.numel() < 4 * N * V
+
+
 def test_autograd_wrapper():
     from hybrid_upcycling_gb300.kl import fused_hidden_state_kl
     w = syn.WORKLOADS["tiny"]
