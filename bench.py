@@ -56,6 +56,49 @@ def whole_job_rate(units_per_rank: int, world: int, steps: int, max_ms: float) -
     return units_per_rank * world * steps / (max_ms / 1e3)
 
 
+def pipelined_e2e(host_in, slots_in, slots_out, copy_out, call, steps, stream, dev):
+    """End-to-end time (ms) of `steps` steps through host memory: every step copies its inputs
+    from the pinned host tensors `host_in` into a device slot, runs `call(inputs, outputs)` on
+    `stream` and copies the `copy_out` outputs back to pinned host memory. Two slots of device
+    inputs and outputs: step k+1's inputs and step k-1's results move on their own copy streams
+    while step k computes."""
+    out_host = {k: torch.empty(slots_out[0][k].shape, dtype=slots_out[0][k].dtype, pin_memory=True)
+                for k in copy_out}
+    cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(cin):  # warm the copy path once
+        for k in host_in:
+            slots_in[0][k].copy_(host_in[k], non_blocking=True)
+    torch.cuda.synchronize()
+    ev = lambda: torch.cuda.Event(enable_timing=False)
+    ev_in, ev_comp, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cin)
+    for i in range(steps):
+        s = i % 2
+        with torch.cuda.stream(cin):
+            if i >= 2:
+                cin.wait_event(ev_comp[s])  # step i-2 has finished reading slot s
+            for k in host_in:
+                slots_in[s][k].copy_(host_in[k], non_blocking=True)
+            ev_in[s].record(cin)
+        stream.wait_event(ev_in[s])
+        if i >= 2:
+            stream.wait_event(ev_out[s])  # step i-2's results have left slot s
+        with torch.cuda.stream(stream):
+            call(slots_in[s], slots_out[s])
+            ev_comp[s].record(stream)
+        with torch.cuda.stream(cout):
+            cout.wait_event(ev_comp[s])
+            for k in copy_out:
+                out_host[k].copy_(slots_out[s][k], non_blocking=True)
+            ev_out[s].record(cout)
+    e1.record(cout)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+    return ms, d2h
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -356,25 +399,23 @@ def run_logits(args, w, rank, world, local):
         host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in z.items()}
         for k in z:
             host[k].copy_(z[k])
-        dz_host = torch.empty(dz.shape, dtype=dz.dtype, pin_memory=True)
-        zd = {k: torch.empty_like(v) for k, v in z.items()}
+        slots_in = [{k: torch.empty_like(v) for k, v in z.items()} for _ in range(2)]
+        slots_out = [{"kl": torch.empty_like(kl), "lse_s": torch.empty_like(ls), "lse_t": torch.empty_like(lt),
+                      "loss": torch.empty_like(loss), "dz": torch.empty_like(dz)} for _ in range(2)]
         n_e2e = max(2, min(args.steps, 5))
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(n_e2e):
-                for k in z:
-                    zd[k].copy_(host[k], non_blocking=True)
-                step(zd)
-                dz_host.copy_(dz, non_blocking=True)
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        ms, d2h = pipelined_e2e(
+            host, slots_in, slots_out, ("loss", "dz"),
+            lambda xi, xo: _lib.hylo_fused_kl_logits(xi["z_s"], xi["z_t"], w.tau, 1.0, xo["kl"], xo["lse_s"],
+                                                     xo["lse_t"], xo["loss"], xo["dz"], stream=stream),
+            n_e2e, stream, dev)
+        _lib.hylo_kl_sync_status(stream)
+        ms = max_over_ranks(ms, world, dev)
         e2e = {"value": whole_job_rate(w.N, world, n_e2e, ms), "unit": "tokens/s",
                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
-               "d2h_bytes_per_step": dz_host.numel() * dz_host.element_size(), "steps": n_e2e,
-               "api": "hylo_fused_kl_logits (C ABI) with pinned-host logits and gradient"}
+               "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "api": "hylo_fused_kl_logits (C ABI) with pinned-host logits and gradient, "
+                      "copies double-buffered on their own streams"}
+        del host, slots_in, slots_out
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import kl_oracle as orc
@@ -439,32 +480,25 @@ def run_ild(args, rank, world, local):
     achieved = alg / (float(np.mean(per)) / 1e3) / 1e9
     e2e = None
     if not args.no_e2e:
-        S_h = torch.empty(S.shape, dtype=S.dtype, pin_memory=True)
-        T_h = torch.empty(T.shape, dtype=T.dtype, pin_memory=True)
-        S_h.copy_(S)
-        T_h.copy_(T)
-        dS_h = torch.empty(dS.shape, dtype=dS.dtype, pin_memory=True)
-        loss_h = torch.empty(1, pin_memory=True)
-        Sd, Td = torch.empty_like(S), torch.empty_like(T)
+        host_in = {"S": torch.empty(S.shape, dtype=S.dtype, pin_memory=True),
+                   "T": torch.empty(T.shape, dtype=T.dtype, pin_memory=True)}
+        host_in["S"].copy_(S)
+        host_in["T"].copy_(T)
+        slots_in = [{"S": torch.empty_like(S), "T": torch.empty_like(T)} for _ in range(2)]
+        slots_out = [{"norms": torch.empty_like(norms), "loss": torch.empty_like(loss), "dS": torch.empty_like(dS)}
+                     for _ in range(2)]
         n_e2e = 5
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(n_e2e):
-                Sd.copy_(S_h, non_blocking=True)
-                Td.copy_(T_h, non_blocking=True)
-                _lib.hylo_ild_loss(Sd, Td, 1.0, norms, loss, dS, stream=stream)
-                dS_h.copy_(dS, non_blocking=True)
-                loss_h.copy_(loss, non_blocking=True)
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        ms, d2h = pipelined_e2e(host_in, slots_in, slots_out, ("loss", "dS"),
+                                lambda xi, xo: _lib.hylo_ild_loss(xi["S"], xi["T"], 1.0, xo["norms"], xo["loss"],
+                                                                  xo["dS"], stream=stream),
+                                n_e2e, stream, dev)
+        _lib.hylo_kl_sync_status(stream)
+        ms = max_over_ranks(ms, world, dev)
         e2e = {"value": whole_job_rate(N, world, n_e2e, ms), "unit": "tokens/s",
-               "h2d_bytes_per_step": 2 * S.numel() * S.element_size(),
-               "d2h_bytes_per_step": dS.numel() * dS.element_size() + 4, "steps": n_e2e,
-               "api": "hylo_ild_loss (C ABI) with pinned-host states, gradient and loss"}
-        del Sd, Td, S_h, T_h, dS_h
+               "h2d_bytes_per_step": 2 * S.numel() * S.element_size(), "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "api": "hylo_ild_loss (C ABI) with pinned-host states, gradient and loss, "
+                      "copies double-buffered on their own streams"}
+        del host_in, slots_in, slots_out
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import kl_oracle as orc
@@ -576,57 +610,25 @@ def main():
     e2e = None
     if not args.no_e2e:
         # Every step copies its inputs in from pinned host memory and its results (kl, loss, dh_s,
-        # dW_s) out, double-buffered: the copies of step k+1's inputs and of step k-1's results
-        # run on their own streams while step k computes.
+        # dW_s) out (double-buffered, see pipelined_e2e).
         host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in x.items()}
         for k in x:
             host[k].copy_(x[k])
-        outs = ("kl", "loss", "dh", "dW")
         xd = [{k: torch.empty_like(v) for k, v in x.items()} for _ in range(2)]
-        bo = [b, {k: (v if k == "ws" else torch.empty_like(v)) for k, v in b.items()}]
-        out_host = [{k: torch.empty(b[k].shape, dtype=b[k].dtype, pin_memory=True) for k in outs} for _ in range(2)]
+        bo = [b, {k: (v if k == "ws" else torch.empty_like(v)) for k, v in b.items()}]  # one shared workspace
         h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = sum(v.numel() * v.element_size() for v in out_host[0].values())
         e2e_steps = max(2, min(args.steps, 5))
-        cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        with torch.cuda.stream(cin):
-            for k in x:  # warm the copy path once
-                xd[0][k].copy_(host[k], non_blocking=True)
-        torch.cuda.synchronize()
         barrier()
-        ev = lambda: torch.cuda.Event(enable_timing=False)
-        ev_in, ev_comp, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(cin)
-        for i in range(e2e_steps):
-            s = i % 2
-            with torch.cuda.stream(cin):
-                if i >= 2:
-                    cin.wait_event(ev_comp[s])  # step i-2 has finished reading slot s
-                for k in x:
-                    xd[s][k].copy_(host[k], non_blocking=True)
-                ev_in[s].record(cin)
-            stream.wait_event(ev_in[s])
-            if i >= 2:
-                stream.wait_event(ev_out[s])  # step i-2's results have left slot s
-            with torch.cuda.stream(stream):
-                step(w, xd[s], bo[s], stream)
-                ev_comp[s].record(stream)
-            with torch.cuda.stream(cout):
-                cout.wait_event(ev_comp[s])
-                for k in outs:
-                    out_host[s][k].copy_(bo[s][k], non_blocking=True)
-                ev_out[s].record(cout)
-        e1.record(cout)
-        torch.cuda.synchronize()
+        e2e_ms, d2h = pipelined_e2e(host, xd, bo, ("kl", "loss", "dh", "dW"),
+                                    lambda xi, xo: step(w, xi, xo, stream), e2e_steps, stream, dev)
         barrier()
         _lib.hylo_kl_sync_status(stream)
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
         e2e = {"value": whole_job_rate(w.N, world, e2e_steps, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "api": "hylo_kl_forward + hylo_kl_backward (C ABI) with pinned-host inputs/outputs, "
                       "copies double-buffered on their own streams"}
-        del xd, host, out_host, bo
+        del xd, host, bo
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
