@@ -250,11 +250,19 @@ def time_repeated(fn, min_s: float = 10.0, max_calls: int = 10000):
             return calls, dt
 
 
+def sample_rows(n_rows: int, count: int) -> torch.Tensor:
+    """min(count, n_rows) row indices spread evenly over [0, n_rows), all in range."""
+    count = max(1, min(count, n_rows))
+    return torch.arange(count) * (n_rows // count)
+
+
 def cpu_oracle_rate(w, x, sample_tokens: int, repeats: int = 1):
     """Times the fp64 oracle (forward + backward, as it stands) on `sample_tokens` tokens of the
-    workload with the full vocabulary and hidden sizes; returns tokens/s."""
+    workload (at most all of them) with the full vocabulary and hidden sizes; returns
+    (tokens/s, seconds)."""
     from oracle import kl_oracle as orc
-    rows = torch.arange(sample_tokens) * max(1, w.N // sample_tokens)
+    rows = sample_rows(w.N, sample_tokens)
+    sample_tokens = len(rows)
     hs = x["h_s"][rows.to(x["h_s"].device)].double().cpu().numpy()
     ht = x["h_t"][rows.to(x["h_t"].device)].double().cpu().numpy()
     Ws = x["W_s"].double().cpu().numpy()
@@ -275,7 +283,7 @@ def run_reference(args, w, rank, world):
     from oracle import kl_oracle as orc
     torch.manual_seed(0)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    tokens = args.ref_tokens
+    tokens = min(args.ref_tokens, w.N)
     if args.path == "hidden":
         x = syn.make_inputs(w, device=dev)
         one = lambda: cpu_oracle_rate(w, x, tokens)[1]
@@ -283,7 +291,7 @@ def run_reference(args, w, rank, world):
         sample = f"{tokens} tokens of {w.name} per step (full V={w.V}, d_s={w.d_s}, d_t={w.d_t}), fp64 numpy"
     elif args.path == "logits":
         z = syn.make_logits(w, device=dev)
-        rows = torch.arange(tokens) * max(1, w.N // tokens)
+        rows = sample_rows(w.N, tokens)
         zs_h = z["z_s"][rows.to(z["z_s"].device)].double().cpu().numpy()
         zt_h = z["z_t"][rows.to(z["z_t"].device)].double().cpu().numpy()
         del z
@@ -419,7 +427,7 @@ def run_logits(args, w, rank, world, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import kl_oracle as orc
-        rows = torch.arange(0, w.N, max(1, w.N // args.cpu_tokens))[: args.cpu_tokens]
+        rows = sample_rows(w.N, args.cpu_tokens)
         zs_h = z["z_s"][rows.to(dev)].double().cpu().numpy()
         zt_h = z["z_t"][rows.to(dev)].double().cpu().numpy()
         calls, dt = time_repeated(lambda: orc.kl_from_logits(zs_h, zt_h, w.tau))
@@ -633,10 +641,11 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res = []
-        calls, dt = time_repeated(lambda: res.append(cpu_oracle_rate(w, x, args.cpu_tokens)[1]))
-        rate = args.cpu_tokens * calls / sum(res)
+        n_s = len(sample_rows(w.N, args.cpu_tokens))
+        calls, dt = time_repeated(lambda: res.append(cpu_oracle_rate(w, x, n_s)[1]))
+        rate = n_s * calls / sum(res)
         cpu = {"value": rate, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-               "sample": f"{calls} x {args.cpu_tokens} tokens of {w.name} (full V and d), fp64 numpy "
+               "sample": f"{calls} x {n_s} tokens of {w.name} (full V and d), fp64 numpy "
                          f"forward+backward, {sum(res):.1f} s"}
 
     if rank == 0:

@@ -49,3 +49,19 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(12.5, 1, torch.device("cpu")) == 12.5
     assert bench.whole_job_rate(100, 1, 10, 1000.0) == pytest.approx(1000.0)
+
+
+def test_cpu_samples_stay_in_range():
+    """The CPU-baseline and reference legs sample rows of the workload: never an index past
+    its last token, whatever the requested sample size (the tiny workload has 64 tokens)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from hybrid_upcycling_gb300 import synthetic as syn
+    for n, c in [(64, 256), (64, 48), (8192, 256), (1, 5), (300, 300)]:
+        r = bench.sample_rows(n, c)
+        assert len(r) == min(n, c) and int(r.min()) >= 0 and int(r.max()) < n
+        assert len(set(r.tolist())) == len(r)
+    w = syn.WORKLOADS["tiny"]
+    x = syn.make_inputs(w, device="cpu")
+    rate, dt = bench.cpu_oracle_rate(w, x, 256)  # more than the workload's tokens
+    assert rate > 0 and dt > 0
