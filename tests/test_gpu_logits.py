@@ -84,6 +84,15 @@ def test_dense_parity(N, V, tau, gs, ld):
     check(z_s, z_t, tau, gs, ld=ld, loss_abs=1e-7)
 
 
+@pytest.mark.parametrize("tau", [0.02, 50.0])
+def test_extreme_temperatures(tau):
+    """tau = 0.02: near one-hot distributions, and exp((m_s - m_t)/tau) overflows fp32 on most
+    rows, so the statistics switch to the direct KL form (the 'far' rows); tau = 50: nearly
+    uniform distributions and a tiny KL."""
+    z_s, z_t = logits(200, 3000, seed=77)
+    check(z_s, z_t, tau, 1.0, loss_abs=1e-9)
+
+
 def test_forward_only_matches_and_writes_no_gradient():
     z_s, z_t = logits(100, 3000, seed=2)
     a = run(z_s, z_t, 1.0, grad=False)

@@ -63,7 +63,19 @@ def frob_rel(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
 
 
-def check_dense(x, tau, token_chunk=4096, grad_scale=1.0, loss_abs=0.0, use_gap=True, tol_loss=TOL_LOSS):
+def bf16_g_floor(hs, Ws, ht, Wt, tau, grad_scale, dh, dW):
+    """Gradient errors of the exact G rounded once to bf16 (the backward's G precision)."""
+    G = orc.kl_grad_logits(hs, Ws, ht, Wt, tau, grad_scale, hs.shape[0])
+    Gb = torch.from_numpy(G).to(torch.bfloat16).double().numpy()
+    return frob_rel(Gb @ Ws, dh), frob_rel(Gb.T @ hs, dW)
+
+
+def check_dense(x, tau, token_chunk=4096, grad_scale=1.0, loss_abs=0.0, use_gap=True, tol_loss=TOL_LOSS,
+                bf16_floor=False):
+    """Every output against the oracle. bf16_floor: cases where each token's gradient is
+    dominated by one or two words, so dh_s / dW_s carry the bf16 rounding of single numbers
+    (up to 2^-8); the gradients are then held to the error of the exact G rounded once to bf16
+    (x 1.1) where that exceeds the 2e-3 bound."""
     g = run(x, tau, token_chunk, grad_scale, use_gap=use_gap)
     hs, Ws, ht, Wt = (f64(x[k]) for k in ("h_s", "W_s", "h_t", "W_t"))
     kl, ls, lt, loss = orc.kl_forward(hs, Ws, ht, Wt, tau)
@@ -77,8 +89,13 @@ def check_dense(x, tau, token_chunk=4096, grad_scale=1.0, loss_abs=0.0, use_gap=
     assert np.all(np.abs(f64(g["lse_t"]) - lt) <= TOL_LSE * (1 + np.abs(lt)))
     if use_gap:  # the gap is at least as accurate as the lse values themselves
         assert np.all(np.abs(f64(g["gap"]) - (ls - lt)) <= TOL_LSE * (1 + np.abs(ls)))
-    assert frob_rel(f64(g["dh"]), dh) <= TOL_GRAD, frob_rel(f64(g["dh"]), dh)
-    assert frob_rel(f64(g["dW"]), dW) <= TOL_GRAD, frob_rel(f64(g["dW"]), dW)
+    tol_dh = tol_dW = TOL_GRAD
+    if bf16_floor:
+        f_dh, f_dW = bf16_g_floor(hs, Ws, ht, Wt, tau, grad_scale, dh, dW)
+        tol_dh, tol_dW = max(TOL_GRAD, 1.1 * f_dh), max(TOL_GRAD, 1.1 * f_dW)
+        print(f"bf16-G floor: dh {f_dh:.2e}, dW {f_dW:.2e}")
+    assert frob_rel(f64(g["dh"]), dh) <= tol_dh, frob_rel(f64(g["dh"]), dh)
+    assert frob_rel(f64(g["dW"]), dW) <= tol_dW, frob_rel(f64(g["dW"]), dW)
     return g
 
 
@@ -128,6 +145,15 @@ def test_ragged_shapes(N, d_s, d_t, V, tau, chunk, gs, w_std):
     # over K = 16392 put lse ~1e-3 low, past the 2e-5 (1 + |lse|) bound derived for K <= 4096)
     x = gen(N, d_s, d_t, V, seed=N + V, w_std=w_std)
     check_dense(x, tau, chunk, gs, loss_abs=1e-7)
+
+
+@pytest.mark.parametrize("tau", [0.05, 40.0])
+def test_extreme_temperatures(tau):
+    """Near one-hot (tau = 0.05: exp((m_s - m_t)/tau) overflows fp32, the direct KL form; each
+    token's gradient is then one or two words, held to the bf16-G floor) and nearly uniform
+    (tau = 40: tiny KL) distributions, forward and backward."""
+    x = gen(300, 128, 256, 3000, seed=31, w_std=0.1)
+    check_dense(x, tau, 4096, 1.0, loss_abs=1e-9, bf16_floor=tau < 1)
 
 
 def test_largest_hidden_size():
