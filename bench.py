@@ -207,12 +207,14 @@ def gpu_id(local: int) -> str:
         return str(local)
 
 
-def make_buffers(w, x, dev):
+def make_buffers(w, x, dev, split=False):
     from hybrid_upcycling_gb300 import _lib
     f = dict(dtype=torch.float32, device=dev)
+    wsb = (_lib.hylo_kl_workspace_bytes_split if split else _lib.hylo_kl_workspace_bytes)(w.N, w.d_s, w.d_t, w.V,
+                                                                                          w.token_chunk)
     b = {
-        "ws": torch.empty(_lib.hylo_kl_workspace_bytes(w.N, w.d_s, w.d_t, w.V, w.token_chunk), dtype=torch.uint8,
-                          device=dev),
+        "split": split,
+        "ws": torch.empty(wsb, dtype=torch.uint8, device=dev),
         "kl": torch.empty(w.N, **f), "lse_s": torch.empty(w.N, **f), "lse_t": torch.empty(w.N, **f),
         "gap": torch.empty(w.N, **f),
         "loss": torch.empty(1, **f), "dh": torch.empty(w.N, w.d_s, **f), "dW": torch.empty(w.V, w.d_s, **f),
@@ -228,15 +230,17 @@ def step(w, x, b, stream, ev=None):
                          b["lse_t"], b["loss"], b["ws"], stream=stream, lse_gap=b["gap"])
     if ev is not None:
         ev[1].record(stream)
-    _lib.hylo_kl_backward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, w.token_chunk, b["lse_s"], b["lse_t"], 1.0,
-                          b["dh"], b["dW"], b["ws"], stream=stream, lse_gap=b["gap"])
+    bwd = _lib.hylo_kl_backward_split if b["split"] else _lib.hylo_kl_backward
+    bwd(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, w.token_chunk, b["lse_s"], b["lse_t"], 1.0, b["dh"], b["dW"],
+        b["ws"], stream=stream, lse_gap=b["gap"])
     if ev is not None:
         ev[2].record(stream)
 
 
-def launches_per_step(w) -> int:
+def launches_per_step(w, split: bool = False) -> int:
     chunks = math.ceil(w.N / min(w.token_chunk, w.N))
-    return 3 + 2 * chunks  # fused fwd + combine + mean; per chunk: fused G + paired dh/dW GEMM
+    # fused fwd + combine + mean; per chunk: fused G + paired dh/dW GEMM (+ its low-order pass)
+    return 3 + (3 if split else 2) * chunks
 
 
 def time_repeated(fn, min_s: float = 10.0, max_calls: int = 10000):
@@ -541,6 +545,8 @@ def main():
                          "ild: the Stage-I ILD alignment loss")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--split-g", action="store_true",
+                    help="time hylo_kl_backward_split (G as two bf16 terms) instead of hylo_kl_backward")
     ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample size for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=48, help="oracle tokens per reference-arm step")
     args = ap.parse_args()
@@ -576,7 +582,7 @@ def main():
     _lib.load()
 
     x = syn.make_inputs(w, device=dev)
-    b = make_buffers(w, x, dev)
+    b = make_buffers(w, x, dev, split=args.split_g)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
 
@@ -623,7 +629,8 @@ def main():
         for k in x:
             host[k].copy_(x[k])
         xd = [{k: torch.empty_like(v) for k, v in x.items()} for _ in range(2)]
-        bo = [b, {k: (v if k == "ws" else torch.empty_like(v)) for k, v in b.items()}]  # one shared workspace
+        # one shared workspace (and flags); fresh output buffers for the second slot
+        bo = [b, {k: (torch.empty_like(v) if torch.is_tensor(v) and k != "ws" else v) for k, v in b.items()}]
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         e2e_steps = max(2, min(args.steps, 5))
         barrier()
@@ -652,7 +659,8 @@ def main():
         line = {
             "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w),
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(config_dict(w), **({"g_terms": 2} if args.split_g else {})),
             "tflops": tflops, "tflops_unit": "TFLOP/s (4 N V (2 d_s + d_t) executed flops per step)",
             "pct_of_peak": 100.0 * tflops / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
             "peak_source": peak_src, "fwd_ms": fwd_avg, "bwd_ms": float(np.mean(bwd_ms)), "loss": loss_val,
@@ -660,7 +668,7 @@ def main():
                          "achieved": fwd_tflops, "peak": peak_sus, "unit": "TFLOP/s", "frac": fwd_tflops / peak_sus,
                          "traffic": traffic, "peak_kind": f"bf16_tflops_sustained ({peak_src})",
                          "flops_per_launch": w.flops_fwd()},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step(w) * args.steps,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step(w, args.split_g) * args.steps,
             "clocks": clk.summary(),
             "memory": {"workspace_bytes": int(b["ws"].numel()), "dense_fp32_logits_bytes": 4 * w.N * w.V,
                        "note": "the library allocates nothing; the caller's workspace is its only scratch"},

@@ -28,6 +28,7 @@ STATUS = {
 }
 
 EXPORTS = ("hylo_kl_workspace_bytes", "hylo_kl_forward", "hylo_kl_backward", "hylo_kl_sync_status",
+           "hylo_kl_workspace_bytes_split", "hylo_kl_backward_split",
            "hylo_kl_last_error", "hylo_kl_forward_noalloc", "hylo_kl_selftest_wait_timeout",
            "hylo_fused_kl_logits", "hylo_ild_loss")
 
@@ -56,6 +57,10 @@ def load() -> ctypes.CDLL:
     L.hylo_kl_forward.restype = ctypes.c_int
     L.hylo_kl_backward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, vp, f32, vp, vp, vp, sz, vp]
     L.hylo_kl_backward.restype = ctypes.c_int
+    L.hylo_kl_workspace_bytes_split.argtypes = [i64, i64, i64, i64, i64]
+    L.hylo_kl_workspace_bytes_split.restype = sz
+    L.hylo_kl_backward_split.argtypes = list(L.hylo_kl_backward.argtypes)
+    L.hylo_kl_backward_split.restype = ctypes.c_int
     L.hylo_kl_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, f32, i64, vp, vp, vp, vp, vp, vp]
     L.hylo_kl_forward_noalloc.restype = ctypes.c_int
     L.hylo_fused_kl_logits.argtypes = [vp, vp, i64, i64, i64, f32, f32, vp, vp, vp, vp, vp, vp]
@@ -122,6 +127,20 @@ def hylo_kl_backward(h_s, W_s, h_t, W_t, tau: float, token_chunk: int, lse_s, ls
                                    int(token_chunk), _ptr(lse_s), _ptr(lse_t), _ptr(lse_gap), float(grad_scale),
                                    _ptr(dh_s), _ptr(dW_s), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)))
+
+
+def hylo_kl_workspace_bytes_split(N: int, d_s: int, d_t: int, V: int, token_chunk: int = 4096) -> int:
+    return int(load().hylo_kl_workspace_bytes_split(N, d_s, d_t, V, token_chunk))
+
+
+def hylo_kl_backward_split(h_s, W_s, h_t, W_t, tau: float, token_chunk: int, lse_s, lse_t, grad_scale: float,
+                           dh_s, dW_s, workspace, stream=None, lse_gap=None) -> None:
+    """hylo_kl_backward with G kept as two bf16 terms (workspace: hylo_kl_workspace_bytes_split)."""
+    N, d_s, d_t, V = _dims(h_s, W_s, h_t, W_t)
+    _check(load().hylo_kl_backward_split(_ptr(h_s), _ptr(W_s), _ptr(h_t), _ptr(W_t), N, d_s, d_t, V, float(tau),
+                                         int(token_chunk), _ptr(lse_s), _ptr(lse_t), _ptr(lse_gap), float(grad_scale),
+                                         _ptr(dh_s), _ptr(dW_s), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def hylo_kl_forward_noalloc(h_s, W_s, h_t, W_t, tau: float, token_chunk: int, kl, lse_s, lse_t, loss,

@@ -34,6 +34,7 @@ struct FusedParams {
   const float* lse_t;
   const float* lse_gap;  // backward: precise lse_s - lse_t per token, or null (then lse_s - lse_t)
   float gscale;     // backward: grad_scale / (tau * N_total)
+  int split;        // backward: also store G - bf16(G), rounded to bf16, through the second G map
   WaitCtl ctl;
 };
 
@@ -67,8 +68,8 @@ struct GemmParams {
 // `clusters` clusters, each working through units (256-token tile, vocabulary segment).
 cudaError_t fused_prepare(int bn, int* max_clusters);
 cudaError_t launch_fused(int bn, bool backward, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
-                         const CUtensorMap& Wt, const CUtensorMap& G, const FusedParams& p, int clusters,
-                         cudaStream_t stream);
+                         const CUtensorMap& Wt, const CUtensorMap& G, const CUtensorMap& G2, const FusedParams& p,
+                         int clusters, cudaStream_t stream);
 cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, float* kl, float* lse_s,
                            float* lse_t, float* lse_gap, cudaStream_t stream);
 cudaError_t launch_mean(const float* kl, int N, float* loss, cudaStream_t stream);

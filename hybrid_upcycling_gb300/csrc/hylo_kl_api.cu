@@ -229,6 +229,13 @@ size_t hylo_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V, i
   return f > b ? f : b;
 }
 
+size_t hylo_kl_workspace_bytes_split(int64_t N, int64_t d_s, int64_t d_t, int64_t V, int64_t token_chunk) {
+  g_last_error.clear();
+  if (!sizes_ok(N, d_s, d_t, V)) return 0;
+  const size_t f = round256(fwd_bytes(N)), b = 2 * round256(bwd_bytes(N, V, token_chunk));
+  return f > b ? f : b;
+}
+
 hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t, const uint16_t* W_t,
                             int64_t N, int64_t d_s, int64_t d_t, int64_t V, float tau, int64_t token_chunk,
                             float* kl, float* lse_s, float* lse_t, float* lse_gap, float* loss, void* workspace,
@@ -265,7 +272,7 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
   const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
 
-  cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
+  cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, m_hs, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
   e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, lse_gap, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch combine");
@@ -274,15 +281,22 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
   return HYLO_OK;
 }
 
-hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t, const uint16_t* W_t,
-                             int64_t N, int64_t d_s, int64_t d_t, int64_t V, float tau, int64_t token_chunk,
-                             const float* lse_s, const float* lse_t, const float* lse_gap, float grad_scale,
-                             float* dh_s, float* dW_s,
-                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Both backward entry points. split: G is stored as bf16(G) and bf16(G - bf16(G)) in two
+// halves of the workspace, and each chunk runs the gradient GEMM twice (the second pass adds).
+hylo_status backward_impl(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t, const uint16_t* W_t,
+                          int64_t N, int64_t d_s, int64_t d_t, int64_t V, float tau, int64_t token_chunk,
+                          const float* lse_s, const float* lse_t, const float* lse_gap, float grad_scale,
+                          float* dh_s, float* dW_s, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                          bool split) {
   g_last_error.clear();
   if (!lse_s || !lse_t || !dh_s || !dW_s) return fail(HYLO_ERR_NULL, "an lse or gradient pointer is NULL");
+  const size_t g_bytes = sizes_ok(N, d_s, d_t, V) ? round256(bwd_bytes(N, V, token_chunk)) : 0;
   hylo_status st = check_common(h_s, W_s, h_t, W_t, N, d_s, d_t, V, tau, workspace, workspace_bytes,
-                                sizes_ok(N, d_s, d_t, V) ? bwd_bytes(N, V, token_chunk) : 0);
+                                split ? 2 * g_bytes : g_bytes);
   if (st != HYLO_OK) return st;
   if (!std::isfinite(grad_scale)) return fail(HYLO_ERR_TAU, "grad_scale must be finite");
   if (!aligned(dh_s, 16) || !aligned(dW_s, 16)) return fail(HYLO_ERR_ALIGN, "gradient pointers must be 16-byte aligned");
@@ -294,6 +308,7 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
   const int64_t chunk = chunk_rows(N, token_chunk);
   const int64_t vpad = cdiv(V, 8) * 8;
   uint16_t* G = static_cast<uint16_t*>(workspace);
+  uint16_t* G2 = split ? G + g_bytes / 2 : G;  // second half of the workspace: the low-order term
 
   CUtensorMap m_Ws, m_Wt, m_WsB, m_dW;
   if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, fused_bn() / 2)) != HYLO_OK) return st;
@@ -316,6 +331,12 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
     if ((st = make_map(&m_GT, G, bf, V, R, vpad * 2, 64, kBK)) != HYLO_OK) return st;       // MN-major A of dW
     if ((st = make_map(&m_hsB, hs_c, bf, d_s, R, d_s * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major B of dW
     if ((st = make_map(&m_dh, dh_s + c0 * d_s, f32, d_s, R, d_s * 4, 32, 32)) != HYLO_OK) return st;
+    CUtensorMap m_Gst2 = m_Gst, m_GA2 = m_GA, m_GT2 = m_GT;  // the low-order term's maps (split only)
+    if (split) {
+      if ((st = make_map(&m_Gst2, G2, bf, V, R, vpad * 2, 64, 32)) != HYLO_OK) return st;
+      if ((st = make_map(&m_GA2, G2, bf, V, R, vpad * 2, kBK, kBM)) != HYLO_OK) return st;
+      if ((st = make_map(&m_GT2, G2, bf, V, R, vpad * 2, 64, kBK)) != HYLO_OK) return st;
+    }
 
     FusedParams p{};
     p.N = static_cast<int>(R);
@@ -333,9 +354,10 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
     p.lse_t = lse_t + c0;
     p.lse_gap = lse_gap != nullptr ? lse_gap + c0 : nullptr;
     p.gscale = gscale;
+    p.split = split ? 1 : 0;
     p.ctl = ctl;
     const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
-    cudaError_t e = launch_fused(fused_bn(), true, m_hs, m_Ws, m_ht, m_Wt, m_Gst, p, grid, stream);
+    cudaError_t e = launch_fused(fused_bn(), true, m_hs, m_Ws, m_ht, m_Wt, m_Gst, m_Gst2, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launch fused backward");
 
     GemmParams gp{};
@@ -363,8 +385,35 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uin
     schedule_gemm(gp);
     e = launch_gemm_pair(m_GA, m_WsB, m_dh, m_GT, m_hsB, m_dW, gp, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launch gradient GEMM");
+    if (split) {  // add the low-order term's contributions
+      dh.accumulate = 1;
+      dw.accumulate = 1;
+      e = launch_gemm_pair(m_GA2, m_WsB, m_dh, m_GT2, m_hsB, m_dW, gp, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "launch gradient GEMM (low-order term)");
+    }
   }
   return HYLO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t, const uint16_t* W_t,
+                             int64_t N, int64_t d_s, int64_t d_t, int64_t V, float tau, int64_t token_chunk,
+                             const float* lse_s, const float* lse_t, const float* lse_gap, float grad_scale,
+                             float* dh_s, float* dW_s, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return backward_impl(h_s, W_s, h_t, W_t, N, d_s, d_t, V, tau, token_chunk, lse_s, lse_t, lse_gap, grad_scale, dh_s,
+                       dW_s, workspace, workspace_bytes, stream, false);
+}
+
+hylo_status hylo_kl_backward_split(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t,
+                                   const uint16_t* W_t, int64_t N, int64_t d_s, int64_t d_t, int64_t V, float tau,
+                                   int64_t token_chunk, const float* lse_s, const float* lse_t, const float* lse_gap,
+                                   float grad_scale, float* dh_s, float* dW_s, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream) {
+  return backward_impl(h_s, W_s, h_t, W_t, N, d_s, d_t, V, tau, token_chunk, lse_s, lse_t, lse_gap, grad_scale, dh_s,
+                       dW_s, workspace, workspace_bytes, stream, true);
 }
 
 }  // extern "C"
@@ -558,7 +607,7 @@ extern "C" hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
   const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
 
-  cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, p, grid, stream);
+  cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, m_hs, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
   e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, lse_gap, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch combine");

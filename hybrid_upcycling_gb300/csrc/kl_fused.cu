@@ -92,7 +92,8 @@ template <int BN_, bool BWD>
 __global__ void __launch_bounds__(kThreads, 1)
 fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant__ CUtensorMap tm_Ws,
                 const __grid_constant__ CUtensorMap tm_ht, const __grid_constant__ CUtensorMap tm_Wt,
-                const __grid_constant__ CUtensorMap tm_G, const FusedParams p) {
+                const __grid_constant__ CUtensorMap tm_G, const __grid_constant__ CUtensorMap tm_G2,
+                const FusedParams p) {
   using C = FusedCfg<BN_, BWD>;
   constexpr int BN = C::BN;
   constexpr int HB = C::HB;
@@ -138,6 +139,7 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
     prefetch_tmap(&tm_ht);
     prefetch_tmap(&tm_Wt);
     if (BWD) prefetch_tmap(&tm_G);
+    if (BWD && p.split) prefetch_tmap(&tm_G2);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, 512);
@@ -307,7 +309,7 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
           const uint32_t rowaddr = smem_u32(staging) + lane * 128;
 #pragma unroll 1
           for (int c2 = 0; c2 < HALF / 64; ++c2) {
-            uint32_t pk[2][16];
+            uint32_t pk[2][16], pl[2][16];  // G in bf16 and, split, its bf16 rounding remainder
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               const int c = c2 * 2 + half;
@@ -322,7 +324,9 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
                 const float2 g = __fmul2_rn(prob_diff2(make_float2(zt[2 * j], zt[2 * j + 1]),
                                                        make_float2(zs[2 * j], zs[2 * j + 1]), c2v, nbt, nbs, ngl2),
                                             gs2);
-                pk[half][j] = pack_bf16x2(g.x, g.y);
+                const uint32_t hi = pack_bf16x2(g.x, g.y);
+                pk[half][j] = hi;
+                pl[half][j] = pack_bf16x2(g.x - __uint_as_float(hi << 16), g.y - __uint_as_float(hi & 0xffff0000u));
               }
             }
             if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
@@ -338,6 +342,22 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
             if (lane == 0 && row0 + my_rows < p.N) {
               tma_store_2d(&tm_G, staging, col_base + c2 * 64, row0 + my_rows + q * 32);
               bulk_commit_group();
+            }
+            if (p.split) {  // the remainder through the same staging rows, once the store has read them
+              if (lane == 0) bulk_wait_group_read<0>();
+              __syncwarp();
+#pragma unroll
+              for (int c4 = 0; c4 < 8; ++c4) {
+                const uint32_t chunk = static_cast<uint32_t>(c4 ^ (lane & 7));
+                const uint32_t* src = &pl[c4 >> 2][4 * (c4 & 3)];
+                st_shared_v4(rowaddr + chunk * 16, src[0], src[1], src[2], src[3]);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0 && row0 + my_rows < p.N) {
+                tma_store_2d(&tm_G2, staging, col_base + c2 * 64, row0 + my_rows + q * 32);
+                bulk_commit_group();
+              }
             }
           }
         }
@@ -481,10 +501,11 @@ cudaError_t prepare_one(int* max_clusters) {
 
 template <int BN, bool BWD>
 cudaError_t launch_one(const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht, const CUtensorMap& Wt,
-                       const CUtensorMap& G, const FusedParams& p, int clusters, cudaStream_t stream) {
+                       const CUtensorMap& G, const CUtensorMap& G2, const FusedParams& p, int clusters,
+                       cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config<BN, BWD>(attr, clusters, stream);
-  return cudaLaunchKernelEx(&cfg, fused_kl_kernel<BN, BWD>, hs, Ws, ht, Wt, G, p);
+  return cudaLaunchKernelEx(&cfg, fused_kl_kernel<BN, BWD>, hs, Ws, ht, Wt, G, G2, p);
 }
 
 }  // namespace
@@ -498,11 +519,11 @@ cudaError_t fused_prepare(int bn, int* max_clusters) {
 }
 
 cudaError_t launch_fused(int bn, bool backward, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
-                         const CUtensorMap& Wt, const CUtensorMap& G, const FusedParams& p, int clusters,
-                         cudaStream_t stream) {
+                         const CUtensorMap& Wt, const CUtensorMap& G, const CUtensorMap& G2, const FusedParams& p,
+                         int clusters, cudaStream_t stream) {
   if (bn != kFusedBN) return cudaErrorInvalidValue;
-  return backward ? launch_one<kFusedBN, true>(hs, Ws, ht, Wt, G, p, clusters, stream)
-                  : launch_one<kFusedBN, false>(hs, Ws, ht, Wt, G, p, clusters, stream);
+  return backward ? launch_one<kFusedBN, true>(hs, Ws, ht, Wt, G, G2, p, clusters, stream)
+                  : launch_one<kFusedBN, false>(hs, Ws, ht, Wt, G, G2, p, clusters, stream);
 }
 
 cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, float* kl, float* lse_s,

@@ -97,6 +97,26 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s,
                              float grad_scale, float* dh_s, float* dW_s,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Backward with G kept to ~16 significant bits: G is stored as the sum of two bf16 terms,
+ * bf16(G) and bf16(G - bf16(G)), and each token chunk runs the gradient GEMMs twice (the
+ * second pass adds the low-order term's products). Same arguments and results as
+ * hylo_kl_backward, with a gradient error of ~1e-5 relative instead of the ~1e-3 that one
+ * bf16 rounding of G leaves -- which matters where a token's gradient is dominated by one or
+ * two words (near one-hot distributions, or a student that differs from its teacher on few
+ * words), where one rounding alone can exceed 2e-3. Costs one more gradient GEMM per chunk
+ * and twice the backward part of the workspace: pass at least
+ * hylo_kl_workspace_bytes_split(...) bytes. (The pages describe no such variant; it is a
+ * precision option of this library.) */
+size_t hylo_kl_workspace_bytes_split(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
+                                     int64_t token_chunk);
+hylo_status hylo_kl_backward_split(const uint16_t* h_s, const uint16_t* W_s,
+                                   const uint16_t* h_t, const uint16_t* W_t,
+                                   int64_t N, int64_t d_s, int64_t d_t, int64_t V,
+                                   float tau, int64_t token_chunk,
+                                   const float* lse_s, const float* lse_t, const float* lse_gap,
+                                   float grad_scale, float* dh_s, float* dW_s,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Forward that allocates nothing and takes no workspace. (The pages describe no such call;
  * it has no counterpart there.) It is for callers that cannot allocate device memory: a
  * plugin that may only use the buffers its host framework hands it, or a loop that must not

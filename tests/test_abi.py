@@ -136,3 +136,20 @@ def _ild(lib, **kw):
 def test_ild_rejects_bad_arguments(lib, kw, status):
     assert _ild(lib, **kw) == status
     assert lib.hylo_kl_last_error()
+
+
+def test_split_workspace_and_rejection(lib):
+    N, d_s, d_t, V = 8192, 2048, 4096, 128256
+    one = _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096)
+    two = _lib.hylo_kl_workspace_bytes_split(N, d_s, d_t, V, 4096)
+    g = ((4096 * V * 2 + 255) // 256) * 256
+    assert one == g and two == 2 * g
+    # few tokens: the forward's O(N) statistics dominate both
+    assert _lib.hylo_kl_workspace_bytes_split(64, 64, 64, 100, 4096) == 6 * 32 * 64 * 4
+    a = dict(h_s=FAKE, W_s=FAKE, h_t=FAKE, W_t=FAKE, N=16, d_s=64, d_t=128, V=100, tau=1.0, chunk=4096,
+             lse_s=FAKE, lse_t=FAKE, gap=None, gs=1.0, dh=FAKE, dW=FAKE, ws=FAKE, stream=None)
+    small = _lib.hylo_kl_workspace_bytes(4096, 64, 128, 100000, 4096)
+    st = lib.hylo_kl_backward_split(a["h_s"], a["W_s"], a["h_t"], a["W_t"], 4096, 64, 128, 100000, 1.0, 4096,
+                                    a["lse_s"], a["lse_t"], None, 1.0, a["dh"], a["dW"], a["ws"], small, None)
+    assert st == -5  # the single-G workspace is too small for the split backward
+    assert _lib.hylo_kl_workspace_bytes_split(0, 64, 64, 10, 4096) == 0
