@@ -308,13 +308,14 @@ def test_library_allocates_no_device_memory():
     assert ws.numel() < 4 * N * V
 
 
-def test_autograd_wrapper():
+@pytest.mark.parametrize("split_g", [False, True])
+def test_autograd_wrapper(split_g):
     from hybrid_upcycling_gb300.kl import fused_hidden_state_kl
     w = syn.WORKLOADS["tiny"]
     x = syn.make_inputs(w, device="cuda")
     h_s = x["h_s"].clone().requires_grad_(True)
     W_s = x["W_s"].clone().requires_grad_(True)
-    loss, kl = fused_hidden_state_kl(h_s, W_s, x["h_t"], x["W_t"], 1.0)
+    loss, kl = fused_hidden_state_kl(h_s, W_s, x["h_t"], x["W_t"], 1.0, split_g=split_g)
     (2.0 * loss).backward()
     ref = orc.kl_backward(f64(x["h_s"]), f64(x["W_s"]), f64(x["h_t"]), f64(x["W_t"]), 1.0, grad_scale=2.0)
     # the wrapper returns bf16 gradients (the input dtype): allow bf16 rounding on top
