@@ -260,17 +260,22 @@ def sample_rows(n_rows: int, count: int) -> torch.Tensor:
     return torch.arange(count) * (n_rows // count)
 
 
-def cpu_oracle_rate(w, x, sample_tokens: int, repeats: int = 1):
+def oracle_inputs(w, x, sample_tokens: int):
+    """The oracle's fp64 host copies of `sample_tokens` rows of h (at most all of them) and of
+    the full LM heads, widened once outside any timed region."""
+    rows = sample_rows(w.N, sample_tokens)
+    widen = lambda t: t.double().cpu().numpy()
+    return (widen(x["h_s"][rows.to(x["h_s"].device)]), widen(x["W_s"]),
+            widen(x["h_t"][rows.to(x["h_t"].device)]), widen(x["W_t"]))
+
+
+def cpu_oracle_rate(w, x, sample_tokens: int, repeats: int = 1, inputs=None):
     """Times the fp64 oracle (forward + backward, as it stands) on `sample_tokens` tokens of the
     workload (at most all of them) with the full vocabulary and hidden sizes; returns
-    (tokens/s, seconds)."""
+    (tokens/s, seconds). `inputs` (from oracle_inputs) skips re-widening the operands."""
     from oracle import kl_oracle as orc
-    rows = sample_rows(w.N, sample_tokens)
-    sample_tokens = len(rows)
-    hs = x["h_s"][rows.to(x["h_s"].device)].double().cpu().numpy()
-    ht = x["h_t"][rows.to(x["h_t"].device)].double().cpu().numpy()
-    Ws = x["W_s"].double().cpu().numpy()
-    Wt = x["W_t"].double().cpu().numpy()
+    hs, Ws, ht, Wt = inputs if inputs is not None else oracle_inputs(w, x, sample_tokens)
+    sample_tokens = hs.shape[0]
     t0 = time.perf_counter()
     for _ in range(repeats):
         orc.kl_forward(hs, Ws, ht, Wt, w.tau, w.token_chunk)
@@ -290,7 +295,9 @@ def run_reference(args, w, rank, world):
     tokens = min(args.ref_tokens, w.N)
     if args.path == "hidden":
         x = syn.make_inputs(w, device=dev)
-        one = lambda: cpu_oracle_rate(w, x, tokens)[1]
+        prepared = oracle_inputs(w, x, tokens)
+        del x
+        one = lambda: cpu_oracle_rate(w, None, tokens, inputs=prepared)[1]
         metric, config = METRIC, config_dict(w)
         sample = f"{tokens} tokens of {w.name} per step (full V={w.V}, d_s={w.d_s}, d_t={w.d_t}), fp64 numpy"
     elif args.path == "logits":
@@ -649,7 +656,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res = []
         n_s = len(sample_rows(w.N, args.cpu_tokens))
-        calls, dt = time_repeated(lambda: res.append(cpu_oracle_rate(w, x, n_s)[1]))
+        prepared = oracle_inputs(w, x, n_s)
+        calls, dt = time_repeated(lambda: res.append(cpu_oracle_rate(w, x, n_s, inputs=prepared)[1]))
         rate = n_s * calls / sum(res)
         cpu = {"value": rate, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                "sample": f"{calls} x {n_s} tokens of {w.name} (full V and d), fp64 numpy "

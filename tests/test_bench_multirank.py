@@ -65,3 +65,6 @@ def test_cpu_samples_stay_in_range():
     x = syn.make_inputs(w, device="cpu")
     rate, dt = bench.cpu_oracle_rate(w, x, 256)  # more than the workload's tokens
     assert rate > 0 and dt > 0
+    prepared = bench.oracle_inputs(w, x, 256)
+    assert prepared[0].shape == (w.N, w.d_s) and prepared[1].shape == (w.V, w.d_s)
+    assert bench.cpu_oracle_rate(w, None, 256, inputs=prepared)[0] > 0
