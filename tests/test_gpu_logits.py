@@ -93,6 +93,22 @@ def test_extreme_temperatures(tau):
     check(z_s, z_t, tau, 1.0, loss_abs=1e-9)
 
 
+@pytest.mark.parametrize("V,grad", [(64, True), (64, False), (8, True), (1000, False)])
+def test_many_short_rows(V, grad):
+    """Thousands of rows of one chunk each: warps turn rows over fast and may run ahead of the
+    row's merging warp by several rows, which the slot barriers (partials, row values) must
+    hold back; every row against the oracle, with and without the gradient pass."""
+    z_s, z_t = logits(6000, V, seed=V + 3)
+    if grad:
+        check(z_s, z_t, 1.0, 1.0, loss_abs=1e-9)
+    else:
+        g = run(z_s, z_t, 1.0, grad=False)
+        kl, ls, lt, loss, _ = orc.kl_from_logits(f64(z_s), f64(z_t), 1.0)
+        assert np.all(np.abs(f64(g["kl"]) - kl) <= TOL_KL * (1 + kl))
+        assert np.all(np.abs(f64(g["lse_s"]) - ls) <= TOL_LSE * (1 + np.abs(ls)))
+        assert abs(g["loss"].item() - loss) <= TOL_LOSS * loss
+
+
 def test_forward_only_matches_and_writes_no_gradient():
     z_s, z_t = logits(100, 3000, seed=2)
     a = run(z_s, z_t, 1.0, grad=False)
