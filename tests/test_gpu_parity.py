@@ -140,6 +140,7 @@ def test_rational_golden_case():
     (129, 64, 64, 257, 1.0, 4096, 1.0, 0.1),         # one row and one column past a tile
     (1, 8, 8, 3, 1.0, 4096, 1.0, 0.1),               # minimum sizes
     (300, 8192, 16392, 2000, 1.0, 4096, 1.0, 0.01),  # wide hidden states (a 70B-class teacher), ragged K
+    (20000, 64, 64, 300, 1.0, 4096, 1.0, 0.1),       # many short units: 2 vocabulary tiles, 5 chunks
 ])
 def test_ragged_shapes(N, d_s, d_t, V, tau, chunk, gs, w_std):
     # w_std keeps the logits' spread near the workloads' (std ~1.3 at the wide shapes): the
