@@ -148,6 +148,9 @@ size_t bwd_bytes(int64_t N, int64_t V, int64_t token_chunk) {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// The fused kernels' pacing counters (one per cluster) follow the statistics or G region.
+constexpr size_t kProgressBytes = kMaxClusters * sizeof(unsigned long long);
+
 // Number of vocabulary segments per pair tile: the work units (256-token tile, segment) are
 // dealt round-robin to the persistent CTA pairs, so pick the split that minimises
 // waves x (vocab tiles per segment), with a small cost per extra segment.
@@ -226,14 +229,14 @@ size_t hylo_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V, i
   g_last_error.clear();
   if (!sizes_ok(N, d_s, d_t, V)) return 0;
   const size_t f = round256(fwd_bytes(N)), b = round256(bwd_bytes(N, V, token_chunk));
-  return f > b ? f : b;
+  return (f > b ? f : b) + kProgressBytes;
 }
 
 size_t hylo_kl_workspace_bytes_split(int64_t N, int64_t d_s, int64_t d_t, int64_t V, int64_t token_chunk) {
   g_last_error.clear();
   if (!sizes_ok(N, d_s, d_t, V)) return 0;
   const size_t f = round256(fwd_bytes(N)), b = 2 * round256(bwd_bytes(N, V, token_chunk));
-  return f > b ? f : b;
+  return (f > b ? f : b) + kProgressBytes;
 }
 
 hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t, const uint16_t* W_t,
@@ -243,8 +246,9 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
   g_last_error.clear();
   (void)token_chunk;  // the forward needs O(N) scratch whatever the chunk
   if (!kl || !lse_s || !lse_t || !loss) return fail(HYLO_ERR_NULL, "an output pointer is NULL");
+  const size_t stats_bytes = sizes_ok(N, d_s, d_t, V) ? round256(fwd_bytes(N)) : 0;
   hylo_status st = check_common(h_s, W_s, h_t, W_t, N, d_s, d_t, V, tau, workspace, workspace_bytes,
-                                sizes_ok(N, d_s, d_t, V) ? fwd_bytes(N) : 0);
+                                stats_bytes + kProgressBytes);
   if (st != HYLO_OK) return st;
   DeviceState* dev = nullptr;
   if ((st = current_device(&dev)) != HYLO_OK) return st;
@@ -269,10 +273,13 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
   p.c = 1.4426950408889634f / tau;
   p.inv_tau = 1.0f / tau;
   p.part = static_cast<float*>(workspace);
+  p.progress = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + stats_bytes);
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
   const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
 
-  cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, m_hs, p, grid, stream);
+  cudaError_t e = cudaMemsetAsync(p.progress, 0, kProgressBytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clear pacing counters");
+  e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, m_hs, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
   e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, lse_gap, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch combine");
@@ -295,8 +302,9 @@ hylo_status backward_impl(const uint16_t* h_s, const uint16_t* W_s, const uint16
   g_last_error.clear();
   if (!lse_s || !lse_t || !dh_s || !dW_s) return fail(HYLO_ERR_NULL, "an lse or gradient pointer is NULL");
   const size_t g_bytes = sizes_ok(N, d_s, d_t, V) ? round256(bwd_bytes(N, V, token_chunk)) : 0;
+  const size_t g_total = split ? 2 * g_bytes : g_bytes;
   hylo_status st = check_common(h_s, W_s, h_t, W_t, N, d_s, d_t, V, tau, workspace, workspace_bytes,
-                                split ? 2 * g_bytes : g_bytes);
+                                g_total + kProgressBytes);
   if (st != HYLO_OK) return st;
   if (!std::isfinite(grad_scale)) return fail(HYLO_ERR_TAU, "grad_scale must be finite");
   if (!aligned(dh_s, 16) || !aligned(dW_s, 16)) return fail(HYLO_ERR_ALIGN, "gradient pointers must be 16-byte aligned");
@@ -355,9 +363,12 @@ hylo_status backward_impl(const uint16_t* h_s, const uint16_t* W_s, const uint16
     p.lse_gap = lse_gap != nullptr ? lse_gap + c0 : nullptr;
     p.gscale = gscale;
     p.split = split ? 1 : 0;
+    p.progress = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + g_total);
     p.ctl = ctl;
     const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
-    cudaError_t e = launch_fused(fused_bn(), true, m_hs, m_Ws, m_ht, m_Wt, m_Gst, m_Gst2, p, grid, stream);
+    cudaError_t e = cudaMemsetAsync(p.progress, 0, kProgressBytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clear pacing counters");
+    e = launch_fused(fused_bn(), true, m_hs, m_Ws, m_ht, m_Wt, m_Gst, m_Gst2, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launch fused backward");
 
     GemmParams gp{};
@@ -604,6 +615,7 @@ extern "C" hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16
   p.c = 1.4426950408889634f / tau;
   p.inv_tau = 1.0f / tau;
   p.part = scratch;  // every (segment, token) slot read by the combine step is written first
+  p.progress = nullptr;  // no pacing: the built-in scratch holds the statistics only
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
   const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
 

@@ -37,16 +37,19 @@ def test_exports_every_declared_symbol(lib):
     assert set(_lib.EXPORTS) <= names
 
 
+PACE = 128 * 8  # the fused kernels' pacing counters, one 8-byte word per cluster
+
+
 def test_workspace_bytes(lib):
     N, d_s, d_t, V = 65536, 2048, 4096, 128256
     fwd = 6 * 32 * N * 4
     bwd = 4096 * V * 2
-    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096) == max(fwd, bwd)
+    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096) == max(fwd, bwd) + PACE
     # O(N + token_chunk * V), never N * V
-    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 1024) == max(fwd, 1024 * V * 2)
+    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 1024) == max(fwd, 1024 * V * 2) + PACE
     assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096) < N * V * 2 // 8
     # chunk larger than N is clamped to N; <= 0 means 4096
-    assert _lib.hylo_kl_workspace_bytes(100, 64, 128, 513, 100000) == max(6 * 32 * 100 * 4, ((100 * 520 * 2 + 255) // 256) * 256)
+    assert _lib.hylo_kl_workspace_bytes(100, 64, 128, 513, 100000) == max(6 * 32 * 100 * 4, ((100 * 520 * 2 + 255) // 256) * 256) + PACE
     assert _lib.hylo_kl_workspace_bytes(8192, 64, 64, 1000, 0) == _lib.hylo_kl_workspace_bytes(8192, 64, 64, 1000, 4096)
     # invalid sizes give 0
     assert _lib.hylo_kl_workspace_bytes(0, 64, 64, 10, 4096) == 0
@@ -143,9 +146,9 @@ def test_split_workspace_and_rejection(lib):
     one = _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096)
     two = _lib.hylo_kl_workspace_bytes_split(N, d_s, d_t, V, 4096)
     g = ((4096 * V * 2 + 255) // 256) * 256
-    assert one == g and two == 2 * g
+    assert one == g + PACE and two == 2 * g + PACE
     # few tokens: the forward's O(N) statistics dominate both
-    assert _lib.hylo_kl_workspace_bytes_split(64, 64, 64, 100, 4096) == 6 * 32 * 64 * 4
+    assert _lib.hylo_kl_workspace_bytes_split(64, 64, 64, 100, 4096) == 6 * 32 * 64 * 4 + PACE
     a = dict(h_s=FAKE, W_s=FAKE, h_t=FAKE, W_t=FAKE, N=16, d_s=64, d_t=128, V=100, tau=1.0, chunk=4096,
              lse_s=FAKE, lse_t=FAKE, gap=None, gs=1.0, dh=FAKE, dW=FAKE, ws=FAKE, stream=None)
     small = _lib.hylo_kl_workspace_bytes(4096, 64, 128, 100000, 4096)

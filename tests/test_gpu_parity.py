@@ -304,8 +304,9 @@ def test_library_allocates_no_device_memory():
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0, (free0, free1)
-    # O(N) statistics or one chunk's bf16 G, whichever is larger; below one model's fp32 logits
-    assert ws.numel() <= max(6 * 32 * N * 4, chunk * ((V + 7) // 8 * 8) * 2) + 256
+    # O(N) statistics or one chunk's bf16 G, whichever is larger (+ 1 KB of pacing counters);
+    # below one model's fp32 logits
+    assert ws.numel() <= max(6 * 32 * N * 4, chunk * ((V + 7) // 8 * 8) * 2) + 256 + 128 * 8
     assert ws.numel() < 4 * N * V
 
 
