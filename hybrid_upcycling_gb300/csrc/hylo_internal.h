@@ -35,7 +35,7 @@ struct FusedParams {
   const float* lse_gap;  // backward: precise lse_s - lse_t per token, or null (then lse_s - lse_t)
   float gscale;     // backward: grad_scale / (tau * N_total)
   int split;        // backward: also store G - bf16(G), rounded to bf16, through the second G map
-  unsigned long long* progress;  // per-cluster pacing counters [kMaxClusters], zero at launch; null: no pacing
+  unsigned long long* progress;  // pacing counters [kMaxClusters] + off switch, zero at launch; null: no pacing
   WaitCtl ctl;
 };
 

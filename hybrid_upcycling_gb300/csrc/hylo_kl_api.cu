@@ -148,8 +148,9 @@ size_t bwd_bytes(int64_t N, int64_t V, int64_t token_chunk) {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// The fused kernels' pacing counters (one per cluster) follow the statistics or G region.
-constexpr size_t kProgressBytes = kMaxClusters * sizeof(unsigned long long);
+// The fused kernels' pacing counters (one per cluster, then the switch that turns pacing off)
+// follow the statistics or G region.
+constexpr size_t kProgressBytes = ((kMaxClusters + 1) * sizeof(unsigned long long) + 255) & ~size_t(255);
 
 // Number of vocabulary segments per pair tile: the work units (256-token tile, segment) are
 // dealt round-robin to the persistent CTA pairs, so pick the split that minimises

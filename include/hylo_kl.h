@@ -60,7 +60,7 @@ typedef enum {
 /* Bytes of device workspace that hylo_kl_forward and hylo_kl_backward need for these sizes.
  * It is O(N) for the forward (per-token partial softmax statistics) and
  * O(token_chunk * V) bf16 for the backward (the gradient of one token chunk's logits),
- * never O(N * V), plus 1 KB of counters with which the fused kernels keep the clusters that
+ * never O(N * V), plus 1.25 KB of counters with which the fused kernels keep the clusters that
  * share LM-head tiles in step (cleared by each call). Returns 0 for invalid sizes.
  * token_chunk <= 0 means 4096. */
 size_t hylo_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V,

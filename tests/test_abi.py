@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(_lib.EXPORTS) <= names
 
 
-PACE = 128 * 8  # the fused kernels' pacing counters, one 8-byte word per cluster
+PACE = 1280  # the fused kernels' pacing counters: one 8-byte word per cluster and a switch, to 256 B
 
 
 def test_workspace_bytes(lib):

@@ -280,6 +280,25 @@ def test_runs_on_a_side_stream():
         assert torch.equal(ref[k], got[k]), k
 
 
+def test_same_results_beside_a_concurrent_kernel():
+    """The fused kernels pace clusters against each other; with another stream's kernels holding
+    SMs, some clusters start late, the pacing gives up (bounded wait) and the results are still
+    the same bits as in a call that ran alone."""
+    x = gen(2048, 256, 512, 20000, seed=17, w_std=0.08)
+    ref = run(x, 1.0, token_chunk=1024)
+    busy, ours = torch.cuda.Stream(), torch.cuda.Stream()
+    a = torch.randn(8192, 8192, device="cuda").to(torch.bfloat16)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(busy):
+        for _ in range(60):
+            a = (a @ a) * 1e-3
+    with torch.cuda.stream(ours):
+        got = run(x, 1.0, token_chunk=1024, stream=ours)
+    torch.cuda.synchronize()
+    for k in ref:
+        assert torch.equal(ref[k], got[k]), k
+
+
 def test_library_allocates_no_device_memory():
     """The caller owns every byte: after a first call on the device (one-time set-up), a
     forward + backward leaves the device's free memory unchanged, so the peak extra memory is
@@ -306,7 +325,7 @@ def test_library_allocates_no_device_memory():
     assert free1 == free0, (free0, free1)
     # O(N) statistics or one chunk's bf16 G, whichever is larger (+ 1 KB of pacing counters);
     # below one model's fp32 logits
-    assert ws.numel() <= max(6 * 32 * N * 4, chunk * ((V + 7) // 8 * 8) * 2) + 256 + 128 * 8
+    assert ws.numel() <= max(6 * 32 * N * 4, chunk * ((V + 7) // 8 * 8) * 2) + 256 + 1280
     assert ws.numel() < 4 * N * V
 
 
