@@ -274,12 +274,15 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
   p.c = 1.4426950408889634f / tau;
   p.inv_tau = 1.0f / tau;
   p.part = static_cast<float*>(workspace);
-  p.progress = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + stats_bytes);
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
   const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
 
-  cudaError_t e = cudaMemsetAsync(p.progress, 0, kProgressBytes, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "clear pacing counters");
+  cudaError_t e = cudaSuccess;
+  if (p.units > grid) {  // pacing matters only when clusters run several units each
+    p.progress = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + stats_bytes);
+    if ((e = cudaMemsetAsync(p.progress, 0, kProgressBytes, stream)) != cudaSuccess)
+      return cuda_fail(e, "clear pacing counters");
+  }
   e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, m_hs, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
   e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, lse_gap, stream);
@@ -364,11 +367,14 @@ hylo_status backward_impl(const uint16_t* h_s, const uint16_t* W_s, const uint16
     p.lse_gap = lse_gap != nullptr ? lse_gap + c0 : nullptr;
     p.gscale = gscale;
     p.split = split ? 1 : 0;
-    p.progress = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + g_total);
     p.ctl = ctl;
     const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
-    cudaError_t e = cudaMemsetAsync(p.progress, 0, kProgressBytes, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "clear pacing counters");
+    cudaError_t e = cudaSuccess;
+    if (p.units > grid) {  // pacing matters only when clusters run several units each
+      p.progress = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + g_total);
+      if ((e = cudaMemsetAsync(p.progress, 0, kProgressBytes, stream)) != cudaSuccess)
+        return cuda_fail(e, "clear pacing counters");
+    }
     e = launch_fused(fused_bn(), true, m_hs, m_Ws, m_ht, m_Wt, m_Gst, m_Gst2, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launch fused backward");
 
