@@ -138,6 +138,7 @@ def test_rational_golden_case():
     (300, 136, 200, 1000, 0.7, 128, 1.0, 0.1),       # ragged everything, 3 chunks
     (1061, 256, 512, 8269, 2.0, 512, 0.37, 0.1),     # several tiles each way, ragged tails
     (129, 64, 64, 257, 1.0, 4096, 1.0, 0.1),         # one row and one column past a tile
+    (129, 64, 64, 257, 1.0, 64, -0.5, 0.1),          # negative upstream gradient, 3 chunks
     (1, 8, 8, 3, 1.0, 4096, 1.0, 0.1),               # minimum sizes
     (300, 8192, 16392, 2000, 1.0, 4096, 1.0, 0.01),  # wide hidden states (a 70B-class teacher), ragged K
     (20000, 64, 64, 300, 1.0, 4096, 1.0, 0.1),       # many short units: 2 vocabulary tiles, 5 chunks
