@@ -444,3 +444,28 @@ def test_split_g_meets_the_bound_where_one_rounding_cannot():
         _, e_dh, e_dW = split_errors(x, tau, 256)
         print(f"split G, tau {tau}: dh {e_dh:.2e}, dW {e_dW:.2e}")
         assert e_dh <= TOL_GRAD_SPLIT and e_dW <= TOL_GRAD_SPLIT, (tau, e_dh, e_dW)
+
+
+def test_split_g_full_size_sampled():
+    """hylo_kl_backward_split at the 8K-token workload's full size: sampled dh_s rows and a
+    dense dW_s on a token subset against the oracle. With G this precise, dh_s's own fp32
+    accumulation over K = V on the tensor cores is what remains: (V/16) 2^-24 = 4.8e-4 of the
+    scale at V = 128256 (the bound the trace identity above uses), still 4x below 2e-3."""
+    w = syn.WORKLOADS["llama1b_8b_8k"]
+    x = syn.make_inputs(w, device="cuda")
+    g = run(x, w.tau, w.token_chunk, split=True)
+    rows = _sample_rows(w.N, w.token_chunk, 64, seed=w.seed + 1)
+    Ws, Wt = f64(x["W_s"]), f64(x["W_t"])
+    _, _, _, dh = orc.kl_rows(f64(x["h_s"][rows]), Ws, f64(x["h_t"][rows]), Wt, w.tau, np.arange(len(rows)),
+                              n_total=w.N)
+    e_dh = frob_rel(f64(g["dh"][rows]), dh)
+    del g
+    torch.cuda.empty_cache()
+    sub = rows[:64]
+    xs = {k: x[k][sub].contiguous() if k.startswith("h") else x[k] for k in x}
+    gs = run(xs, w.tau, w.token_chunk, grad_scale=0.5, split=True)
+    dh_ref, dW_ref = orc.kl_backward(f64(xs["h_s"]), Ws, f64(xs["h_t"]), Wt, w.tau, grad_scale=0.5)
+    e_w = frob_rel(f64(gs["dW"]), dW_ref)
+    print(f"split G full size: dh rows rel {e_dh:.2e}, token-subset dense dW rel {e_w:.2e}")
+    assert e_dh <= max(TOL_GRAD_SPLIT, (w.V / 16) * 2.0 ** -24), e_dh
+    assert e_w <= TOL_GRAD_SPLIT, e_w
