@@ -12,12 +12,13 @@ namespace hylo {
 // Tile sizes shared by host and device code.
 constexpr int kBM = 128;      // token rows per tile (UMMA M, one TMEM lane per row)
 constexpr int kBK = 64;       // k elements per pipeline stage (one 128-byte swizzle row)
-constexpr int kGemmBN = 256;  // output columns per gradient-GEMM pair tile
+constexpr int kGemmBN = 256;  // d_s columns per gradient tile of the backward
 constexpr int kFusedBN = 256; // vocabulary columns per fused pair tile (each CTA stages 128 W rows)
 constexpr int kMaxSegments = 32;
 constexpr int kStatFields = 6; // teacher max, teacher sum, student max, student sum, A, C
 
-// Parameters of the fused dual-GEMM kernel (forward statistics or backward G tiles).
+// Parameters of the fused forward kernel (teacher and student logit tiles folded into
+// per-token softmax/KL statistics).
 struct FusedParams {
   int N;            // token rows covered by the tensor maps of this launch
   int V;            // vocabulary size
@@ -29,48 +30,20 @@ struct FusedParams {
   int units;        // token_tiles * nseg
   float c;          // log2(e) / tau
   float inv_tau;    // 1 / tau
-  float* part;      // forward: partial statistics [kStatFields][nseg][N]
-  const float* lse_s;  // backward: per-token log-sum-exps (natural log of sum exp(z/tau))
-  const float* lse_t;
-  const float* lse_gap;  // backward: precise lse_s - lse_t per token, or null (then lse_s - lse_t)
-  float gscale;     // backward: grad_scale / (tau * N_total)
-  int split;        // backward: also store G - bf16(G), rounded to bf16, through the second G map
-  unsigned long long* progress;  // pacing counters [kMaxClusters] + off switch, zero at launch; null: no pacing
+  float* part;      // partial statistics [kStatFields][nseg][N]
+  unsigned long long* progress;  // pacing counters [kMaxClusters] + off switch; null: no pacing
+  unsigned epoch;   // 1..65535, different from the previous paced launch on the same counters
   WaitCtl ctl;
-};
-
-// One GEMM problem C[M, Nc] (=|+=) sum_k A[m, k] B[n, k] of the paired gradient kernel, tiled
-// in 256 x 256 pair tiles (each CTA of a pair owns 128 rows of the tile).
-struct GemmProblem {
-  int M, Nc;
-  int kblocks;               // ceil(K / 64)
-  int m_tiles, n_tiles, tiles;
-  int a_mn;                  // A operand MN-major (1) or K-major (0); B is MN-major
-  int accumulate;            // 0: overwrite C, 1: add into C (TMA reduce-add)
 };
 
 constexpr int kMaxClusters = 128;
 
-// Both gradient problems of one token chunk. Problem-0 (dh_s, K = V) tiles are dealt
-// round-robin over the clusters. Clusters c >= p0_rem (p0_rem = tiles0 % nclusters, when
-// nonzero) get one problem-0 tile fewer; they first share the problem-1 (dW_s) tiles
-// [0, p1_split) round-robin among themselves, then all clusters share [p1_split, tiles1)
-// round-robin, so concurrently running tiles are neighbours (their G and h_s blocks stay in L2)
-// and every cluster finishes within about one problem-1 tile of the others.
-struct GemmParams {
-  GemmProblem prob[2];
-  int nclusters;
-  int p1_split;
-  WaitCtl ctl;
-};
-
-// Fused dual-GEMM kernel on CTA pairs; bn = vocabulary columns per pair tile (kFusedBN).
+// Fused forward kernel on CTA pairs; bn = vocabulary columns per pair tile (kFusedBN).
 // fused_prepare reports how many 2-CTA clusters fit on the device at once; a launch runs
 // `clusters` clusters, each working through units (256-token tile, vocabulary segment).
 cudaError_t fused_prepare(int bn, int* max_clusters);
-cudaError_t launch_fused(int bn, bool backward, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
-                         const CUtensorMap& Wt, const CUtensorMap& G, const CUtensorMap& G2, const FusedParams& p,
-                         int clusters, cudaStream_t stream);
+cudaError_t launch_fused(int bn, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
+                         const CUtensorMap& Wt, const FusedParams& p, int clusters, cudaStream_t stream);
 cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, float* kl, float* lse_s,
                            float* lse_t, float* lse_gap, cudaStream_t stream);
 cudaError_t launch_mean(const float* kl, int N, float* loss, cudaStream_t stream);
@@ -86,11 +59,38 @@ cudaError_t launch_kl_logits(const uint16_t* zs, const uint16_t* zt, uint16_t* d
 cudaError_t launch_ild(const uint16_t* S, const uint16_t* T, int64_t P, int64_t N, int d, float grad_scale, float* norms,
                        float* loss, uint16_t* dS, int sms, cudaStream_t stream);
 
-// Paired (cta_group::2) gradient GEMM: sets the shared-memory limit and reports how many
-// 2-CTA clusters fit on the device at once; the launch runs p.nclusters clusters.
-int gemm_smem_bytes();
-cudaError_t gemm_prepare(int* max_clusters);
-cudaError_t launch_gemm_pair(const CUtensorMap& A0, const CUtensorMap& B0, const CUtensorMap& C0, const CUtensorMap& A1,
-                             const CUtensorMap& B1, const CUtensorMap& C1, const GemmParams& p, cudaStream_t stream);
+// The backward as one persistent launch (kl_bwd_pipe.cu). The tokens are cut into TB blocks of
+// R rows (R a multiple of 256, or one block of all N) and the vocabulary into VB blocks of bw
+// words (a multiple of 256); block b = (b / VB, b % VB). Per block, "F" work items recompute
+// the block's 256 x 256 logit tile pairs and write G = dL/dz_s (bf16) into ring slot b % kGRing
+// of the workspace, and "M" work items add the block's contributions to dW_s (G^T h_s) and dh_s
+// (G W_s). Items run in the queue order F(0), F(1), M(0), F(2), M(1), F(3), ..., M(B-1), dealt
+// to clusters by an atomic counter; completion counters order M(b) after F(b) and after M(b-1)
+// (same output tiles), and F(b) after M(b - kGRing) (same ring slot).
+constexpr int kGRing = 3;
+struct BwdPipeParams {
+  int N, V, d_s;
+  int kb_s, kb_t;   // 64-wide k-blocks of the student / teacher projections
+  int ntd;          // 256-column tiles of d_s
+  int R, bw;        // token block rows, vocabulary block width
+  int TB, VB, B;    // token blocks, vocabulary blocks, TB * VB
+  float c;          // log2(e) / tau
+  float gscale;     // grad_scale / (tau * N)
+  const float* lse_s;
+  const float* lse_t;
+  const float* lse_gap;  // precise lse_s - lse_t, or null
+  int split;        // also store G - bf16(G) (ring slots kGRing..2 kGRing-1) and add its products
+  unsigned* ctrl;   // [0] work queue, [1] M-item completions, [2 + s] F-item completions of slot s; zero at launch
+  WaitCtl ctl;
+};
+constexpr int kPipeCtrlWords = 2 + kGRing;
+
+// Sets the shared-memory limit and reports how many 2-CTA clusters of the pipelined backward
+// fit on the device at once.
+cudaError_t bwd_pipe_prepare(int* max_clusters);
+// Maps: hs, ht, Ws, Wt K-major (box 64 x 128); WsB, hsB MN-major (box 64 x 64); dh, dW fp32
+// (box 32 x 32); G, GA, GT over the ring [slots][R][bw] bf16 (boxes 64 x 32, 64 x 128, 64 x 64).
+cudaError_t launch_bwd_pipe(const CUtensorMap* maps, const BwdPipeParams& p, int clusters, cudaStream_t stream);
+constexpr int kPipeMaps = 11;
 
 }  // namespace hylo

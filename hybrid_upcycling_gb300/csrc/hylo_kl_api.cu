@@ -27,9 +27,10 @@ struct DeviceState {
   bool init = false;
   bool sm103 = false;
   int sms = 0;
-  int gemm_clusters = 0;   // 2-CTA clusters of the gradient GEMM resident at once
   int fused_clusters = 0;  // 2-CTA clusters of the fused kernels resident at once
   int logits_clusters = 0; // clusters of the logits kernel resident at once
+  int pipe_clusters = 0;   // 2-CTA clusters of the pipelined backward resident at once
+  unsigned pace_epoch = 0;  // epoch of the last paced fused launch on this device
   int* status = nullptr;
   std::string why;
 };
@@ -90,11 +91,11 @@ hylo_status current_device(DeviceState** out) {
       if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
       d.status = static_cast<int*>(p);
       if ((e = fused_prepare(fused_bn(), &d.fused_clusters)) != cudaSuccess ||
-          (e = gemm_prepare(&d.gemm_clusters)) != cudaSuccess || (e = kl_logits_prepare(&d.logits_clusters)) != cudaSuccess)
+          (e = bwd_pipe_prepare(&d.pipe_clusters)) != cudaSuccess ||
+          (e = kl_logits_prepare(&d.logits_clusters)) != cudaSuccess)
         return cuda_fail(e, "kernel set-up");
-      if (d.gemm_clusters < 1 || d.fused_clusters < 1 || d.logits_clusters < 1)
+      if (d.pipe_clusters < 1 || d.fused_clusters < 1 || d.logits_clusters < 1)
         return fail(HYLO_ERR_CUDA, "no thread-block cluster of the kernels fits on the device");
-      if (d.gemm_clusters > kMaxClusters) d.gemm_clusters = kMaxClusters;
       if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
         void* fn = nullptr;
@@ -125,13 +126,51 @@ hylo_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, u
   return HYLO_OK;
 }
 
+// A fresh epoch (1..65535) for a paced fused launch: the pacing counters are never cleared,
+// their words carry the epoch of the launch that wrote them.
+unsigned next_epoch(DeviceState* d) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  d->pace_epoch = d->pace_epoch % 65535u + 1u;
+  return d->pace_epoch;
+}
+
+// 3-D tensor map [outer2][outer1][inner] (contiguous), 128-byte swizzle, zero fill outside.
+hylo_status make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner, uint64_t outer1,
+                        uint64_t outer2, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer1) {
+  cuuint64_t dims[3] = {inner, outer1, outer2};
+  cuuint64_t strides[2] = {row_bytes, row_bytes * outer1};
+  cuuint32_t box[3] = {box_inner, box_outer1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(HYLO_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed with CUresult %d", static_cast<int>(r));
+  return HYLO_OK;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int64_t chunk_rows(int64_t N, int64_t token_chunk) {
+// The backward stages G = dL/dz_s (bf16) in a ring of kGRing blocks of R tokens x bw words:
+// at most kGBlockBytes in all, whatever N, V or token_chunk. R = token_chunk rounded up to a
+// multiple of 256 (at most kMaxBlockTokens, at most N rounded up), so bw is at least
+// kGBlockBytes / (2 kGRing kMaxBlockTokens) = 341 -> 256 words.
+constexpr int64_t kGBlockBytes = int64_t(64) << 20;
+constexpr int64_t kMaxBlockTokens = 32768;
+
+int64_t pipe_rows(int64_t N, int64_t token_chunk) {
   int64_t c = token_chunk <= 0 ? 4096 : token_chunk;
-  return c < N ? c : N;
+  if (c > kMaxBlockTokens) c = kMaxBlockTokens;
+  c = cdiv(c, 256) * 256;
+  const int64_t n = cdiv(N, 256) * 256;
+  return c < n ? c : n;
+}
+
+int64_t pipe_width(int64_t R, int64_t V) {
+  const int64_t w = kGBlockBytes / (kGRing * R * 2) / 256 * 256;
+  const int64_t vmax = cdiv(V, 256) * 256;
+  return w < vmax ? w : vmax;
 }
 
 bool sizes_ok(int64_t N, int64_t d_s, int64_t d_t, int64_t V) {
@@ -141,9 +180,10 @@ bool sizes_ok(int64_t N, int64_t d_s, int64_t d_t, int64_t V) {
 
 size_t fwd_bytes(int64_t N) { return static_cast<size_t>(kStatFields) * kMaxSegments * N * sizeof(float); }
 
+// Bytes of the backward's G ring (one bf16 term): at most kGBlockBytes.
 size_t bwd_bytes(int64_t N, int64_t V, int64_t token_chunk) {
-  const int64_t vpad = cdiv(V, 8) * 8;
-  return static_cast<size_t>(chunk_rows(N, token_chunk)) * vpad * 2;
+  const int64_t R = pipe_rows(N, token_chunk);
+  return static_cast<size_t>(kGRing) * R * pipe_width(R, V) * 2;
 }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -152,54 +192,31 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // follow the statistics or G region.
 constexpr size_t kProgressBytes = ((kMaxClusters + 1) * sizeof(unsigned long long) + 255) & ~size_t(255);
 
+// Pacing matters only when clusters run several units each (units > grid); the counters' words
+// hold the unit index in 24 bits.
+bool pace_launch(int64_t units, int64_t grid) { return units > grid && units / grid < (int64_t(1) << 23); }
+
 // Number of vocabulary segments per pair tile: the work units (256-token tile, segment) are
 // dealt round-robin to the persistent CTA pairs, so pick the split that minimises
 // waves x (vocab tiles per segment), with a small cost per extra segment.
-// Pair tiles per raster group of the fused backward: as many as keep the group's hidden-state
-// tiles (256 rows x (d_s + d_t) bf16 each, re-read for every vocabulary tile) within
-// kGroupBytes of L2. Measured on the 64K workload (DRAM read per launch): backward chunk
-// 10.1 GB with groups of 1 pair tile, 7.8 GB with 16 (3.61 -> 3.56 ms); the forward instead
-// reads least with groups of 1 (229 GB, against 291 / 390 / 402 / 417 GB with 4 / 8 / 16 / 32
-// and 58.7 -> 66.7 ms), so it uses 1.
-constexpr int64_t kGroupBytes = 48ll << 20;
-int raster_group(int64_t d_s, int64_t d_t, int64_t token_tiles) {
-  int64_t g = kGroupBytes / (2 * kBM * (d_s + d_t) * 2);
-  if (g < 1) g = 1;
-  if (g > token_tiles) g = token_tiles;
-  return static_cast<int>(g);
+double segment_cost(int64_t token_tiles, int64_t vtiles, int workers, int s) {
+  const int64_t units = token_tiles * s;
+  const int64_t waves = cdiv(units, workers);
+  const int64_t per = cdiv(vtiles, s);
+  return static_cast<double>(waves * per) * (1.0 + 0.002 * s);
 }
 
 int choose_segments(int64_t token_tiles, int64_t vtiles, int workers) {
   int best = 1;
   double best_cost = 1e300;
   for (int s = 1; s <= kMaxSegments && s <= vtiles; ++s) {
-    const int64_t units = token_tiles * s;
-    const int64_t waves = cdiv(units, workers);
-    const int64_t per = cdiv(vtiles, s);
-    const double cost = static_cast<double>(waves * per) * (1.0 + 0.002 * s);
+    const double cost = segment_cost(token_tiles, vtiles, workers, s);
     if (cost < best_cost) {
       best_cost = cost;
       best = s;
     }
   }
   return best;
-}
-
-// Phase-A size of the paired gradient GEMM schedule (see GemmParams): the clusters holding one
-// problem-0 tile fewer take that tile's worth of problem-1 tiles each before all clusters share
-// the rest.
-void schedule_gemm(GemmParams& gp) {
-  const int ncl = gp.nclusters;
-  const int64_t t0 = gp.prob[0].tiles, t1 = gp.prob[1].tiles;
-  const int64_t k0 = gp.prob[0].kblocks, k1 = gp.prob[1].kblocks > 0 ? gp.prob[1].kblocks : 1;
-  const int64_t rem = t0 % ncl;
-  int64_t split = 0;
-  if (rem != 0) {
-    const int64_t early = ncl - rem;
-    const int64_t per = (k0 + k1 / 2) / k1;  // problem-1 tiles that fill one problem-0 tile's time
-    split = early * per;
-  }
-  gp.p1_split = static_cast<int>(split < t1 ? split : t1);
 }
 
 hylo_status check_common(const void* h_s, const void* W_s, const void* h_t, const void* W_t, int64_t N, int64_t d_s,
@@ -270,20 +287,19 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
   p.vtiles = static_cast<int>(cdiv(V, fused_bn()));
   p.nseg = choose_segments(p.token_tiles, p.vtiles, dev->fused_clusters);
   p.units = p.token_tiles * p.nseg;
-  p.group = 1;  // tile-major: measured least DRAM traffic for the forward (see raster_group)
+  p.group = 1;  // tile-major: least DRAM traffic (measured at 64K: 229 GB per launch against 291-417 GB
+                // for raster groups of 4-32 pair tiles, 58.7 against up to 66.7 ms)
   p.c = 1.4426950408889634f / tau;
   p.inv_tau = 1.0f / tau;
   p.part = static_cast<float*>(workspace);
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
   const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
 
-  cudaError_t e = cudaSuccess;
-  if (p.units > grid) {  // pacing matters only when clusters run several units each
+  if (pace_launch(p.units, grid)) {
     p.progress = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + stats_bytes);
-    if ((e = cudaMemsetAsync(p.progress, 0, kProgressBytes, stream)) != cudaSuccess)
-      return cuda_fail(e, "clear pacing counters");
+    p.epoch = next_epoch(dev);
   }
-  e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, m_hs, p, grid, stream);
+  cudaError_t e = launch_fused(fused_bn(), m_hs, m_Ws, m_ht, m_Wt, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
   e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, lse_gap, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch combine");
@@ -296,8 +312,10 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
 
 namespace {
 
-// Both backward entry points. split: G is stored as bf16(G) and bf16(G - bf16(G)) in two
-// halves of the workspace, and each chunk runs the gradient GEMM twice (the second pass adds).
+// Both backward entry points: one launch of the pipelined backward (kl_bwd_pipe.cu) over
+// token blocks of pipe_rows() tokens and vocabulary blocks of pipe_width() words, with the G
+// ring in the workspace. split: G is also kept as bf16(G - bf16(G)) in a second ring, and each
+// gradient tile accumulates the products of both terms.
 hylo_status backward_impl(const uint16_t* h_s, const uint16_t* W_s, const uint16_t* h_t, const uint16_t* W_t,
                           int64_t N, int64_t d_s, int64_t d_t, int64_t V, float tau, int64_t token_chunk,
                           const float* lse_s, const float* lse_t, const float* lse_gap, float grad_scale,
@@ -312,104 +330,59 @@ hylo_status backward_impl(const uint16_t* h_s, const uint16_t* W_s, const uint16
   if (st != HYLO_OK) return st;
   if (!std::isfinite(grad_scale)) return fail(HYLO_ERR_TAU, "grad_scale must be finite");
   if (!aligned(dh_s, 16) || !aligned(dW_s, 16)) return fail(HYLO_ERR_ALIGN, "gradient pointers must be 16-byte aligned");
+  const int64_t R = pipe_rows(N, token_chunk), bw = pipe_width(R, V);
+  const int64_t TB = cdiv(N, R), VB = cdiv(V, bw), ntd = cdiv(d_s, kGemmBN);
+  // work items: per block, its 256 x 256 G tiles and its dW_s and dh_s tiles (< 2^30 so that
+  // the queue index and the completion counts fit their 32-bit counters)
+  const int64_t items = cdiv(N, 256) * cdiv(V, 256) + (TB * cdiv(V, 256) + VB * cdiv(N, 256)) * ntd;
+  if (items >= (int64_t(1) << 30))
+    return fail(HYLO_ERR_DIM, "N=%lld x V=%lld needs %lld backward work items, more than 2^30",
+                static_cast<long long>(N), static_cast<long long>(V), static_cast<long long>(items));
   DeviceState* dev = nullptr;
   if ((st = current_device(&dev)) != HYLO_OK) return st;
 
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  const int64_t chunk = chunk_rows(N, token_chunk);
-  const int64_t vpad = cdiv(V, 8) * 8;
+  CUtensorMap maps[kPipeMaps];
   uint16_t* G = static_cast<uint16_t*>(workspace);
-  uint16_t* G2 = split ? G + g_bytes / 2 : G;  // second half of the workspace: the low-order term
+  const uint64_t slots = static_cast<uint64_t>(split ? 2 * kGRing : kGRing);
+  if ((st = make_map(&maps[0], h_s, bf, d_s, N, d_s * 2, kBK, kBM)) != HYLO_OK) return st;
+  if ((st = make_map(&maps[1], h_t, bf, d_t, N, d_t * 2, kBK, kBM)) != HYLO_OK) return st;
+  if ((st = make_map(&maps[2], W_s, bf, d_s, V, d_s * 2, kBK, fused_bn() / 2)) != HYLO_OK) return st;
+  if ((st = make_map(&maps[3], W_t, bf, d_t, V, d_t * 2, kBK, fused_bn() / 2)) != HYLO_OK) return st;
+  if ((st = make_map(&maps[4], W_s, bf, d_s, V, d_s * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major B of dh
+  if ((st = make_map(&maps[5], h_s, bf, d_s, N, d_s * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major B of dW
+  if ((st = make_map(&maps[6], dh_s, f32, d_s, N, d_s * 4, 32, 32)) != HYLO_OK) return st;
+  if ((st = make_map(&maps[7], dW_s, f32, d_s, V, d_s * 4, 32, 32)) != HYLO_OK) return st;
+  if ((st = make_map_3d(&maps[8], G, bf, bw, R, slots, bw * 2, 64, 32)) != HYLO_OK) return st;    // G tile stores
+  if ((st = make_map_3d(&maps[9], G, bf, bw, R, slots, bw * 2, kBK, kBM)) != HYLO_OK) return st;  // K-major A of dh
+  if ((st = make_map_3d(&maps[10], G, bf, bw, R, slots, bw * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major A of dW
 
-  CUtensorMap m_Ws, m_Wt, m_WsB, m_dW;
-  if ((st = make_map(&m_Ws, W_s, bf, d_s, V, d_s * 2, kBK, fused_bn() / 2)) != HYLO_OK) return st;
-  if ((st = make_map(&m_Wt, W_t, bf, d_t, V, d_t * 2, kBK, fused_bn() / 2)) != HYLO_OK) return st;
-  if ((st = make_map(&m_WsB, W_s, bf, d_s, V, d_s * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major B of dh
-  if ((st = make_map(&m_dW, dW_s, f32, d_s, V, d_s * 4, 32, 32)) != HYLO_OK) return st;
-
-  const WaitCtl ctl{dev->status, wait_limit_ns()};
-  const float gscale = static_cast<float>(static_cast<double>(grad_scale) / (static_cast<double>(tau) * N));
-
-  for (int64_t c0 = 0; c0 < N; c0 += chunk) {
-    const int64_t R = (N - c0) < chunk ? (N - c0) : chunk;
-    const uint16_t* hs_c = h_s + c0 * d_s;
-    const uint16_t* ht_c = h_t + c0 * d_t;
-    CUtensorMap m_hs, m_ht, m_Gst, m_GA, m_GT, m_hsB, m_dh;
-    if ((st = make_map(&m_hs, hs_c, bf, d_s, R, d_s * 2, kBK, kBM)) != HYLO_OK) return st;
-    if ((st = make_map(&m_ht, ht_c, bf, d_t, R, d_t * 2, kBK, kBM)) != HYLO_OK) return st;
-    if ((st = make_map(&m_Gst, G, bf, V, R, vpad * 2, 64, 32)) != HYLO_OK) return st;       // G tile stores
-    if ((st = make_map(&m_GA, G, bf, V, R, vpad * 2, kBK, kBM)) != HYLO_OK) return st;      // K-major A of dh
-    if ((st = make_map(&m_GT, G, bf, V, R, vpad * 2, 64, kBK)) != HYLO_OK) return st;       // MN-major A of dW
-    if ((st = make_map(&m_hsB, hs_c, bf, d_s, R, d_s * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major B of dW
-    if ((st = make_map(&m_dh, dh_s + c0 * d_s, f32, d_s, R, d_s * 4, 32, 32)) != HYLO_OK) return st;
-    CUtensorMap m_Gst2 = m_Gst, m_GA2 = m_GA, m_GT2 = m_GT;  // the low-order term's maps (split only)
-    if (split) {
-      if ((st = make_map(&m_Gst2, G2, bf, V, R, vpad * 2, 64, 32)) != HYLO_OK) return st;
-      if ((st = make_map(&m_GA2, G2, bf, V, R, vpad * 2, kBK, kBM)) != HYLO_OK) return st;
-      if ((st = make_map(&m_GT2, G2, bf, V, R, vpad * 2, 64, kBK)) != HYLO_OK) return st;
-    }
-
-    FusedParams p{};
-    p.N = static_cast<int>(R);
-    p.V = static_cast<int>(V);
-    p.kb_s = static_cast<int>(cdiv(d_s, kBK));
-    p.kb_t = static_cast<int>(cdiv(d_t, kBK));
-    p.token_tiles = static_cast<int>(cdiv(R, 2 * kBM));
-    p.vtiles = static_cast<int>(cdiv(V, fused_bn()));
-    p.nseg = choose_segments(p.token_tiles, p.vtiles, dev->fused_clusters);
-    p.units = p.token_tiles * p.nseg;
-    p.group = raster_group(d_s, d_t, p.token_tiles);
-    p.c = 1.4426950408889634f / tau;
-    p.inv_tau = 1.0f / tau;
-    p.lse_s = lse_s + c0;
-    p.lse_t = lse_t + c0;
-    p.lse_gap = lse_gap != nullptr ? lse_gap + c0 : nullptr;
-    p.gscale = gscale;
-    p.split = split ? 1 : 0;
-    p.ctl = ctl;
-    const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
-    cudaError_t e = cudaSuccess;
-    if (p.units > grid) {  // pacing matters only when clusters run several units each
-      p.progress = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + g_total);
-      if ((e = cudaMemsetAsync(p.progress, 0, kProgressBytes, stream)) != cudaSuccess)
-        return cuda_fail(e, "clear pacing counters");
-    }
-    e = launch_fused(fused_bn(), true, m_hs, m_Ws, m_ht, m_Wt, m_Gst, m_Gst2, p, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "launch fused backward");
-
-    GemmParams gp{};
-    GemmProblem& dh = gp.prob[0];
-    dh.M = static_cast<int>(R);
-    dh.Nc = static_cast<int>(d_s);
-    dh.kblocks = static_cast<int>(cdiv(V, kBK));
-    dh.m_tiles = static_cast<int>(cdiv(R, 2 * kBM));
-    dh.n_tiles = static_cast<int>(cdiv(d_s, kGemmBN));
-    dh.tiles = dh.m_tiles * dh.n_tiles;
-    dh.a_mn = 0;
-    dh.accumulate = 0;
-    GemmProblem& dw = gp.prob[1];
-    dw.M = static_cast<int>(V);
-    dw.Nc = static_cast<int>(d_s);
-    dw.kblocks = static_cast<int>(cdiv(R, kBK));
-    dw.m_tiles = static_cast<int>(cdiv(V, 2 * kBM));
-    dw.n_tiles = static_cast<int>(cdiv(d_s, kGemmBN));
-    dw.tiles = dw.m_tiles * dw.n_tiles;
-    dw.a_mn = 1;
-    dw.accumulate = c0 > 0 ? 1 : 0;
-    const int64_t all_tiles = static_cast<int64_t>(dh.tiles) + dw.tiles;
-    gp.nclusters = static_cast<int>(all_tiles < dev->gemm_clusters ? all_tiles : dev->gemm_clusters);
-    gp.ctl = ctl;
-    schedule_gemm(gp);
-    e = launch_gemm_pair(m_GA, m_WsB, m_dh, m_GT, m_hsB, m_dW, gp, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "launch gradient GEMM");
-    if (split) {  // add the low-order term's contributions
-      dh.accumulate = 1;
-      dw.accumulate = 1;
-      e = launch_gemm_pair(m_GA2, m_WsB, m_dh, m_GT2, m_hsB, m_dW, gp, stream);
-      if (e != cudaSuccess) return cuda_fail(e, "launch gradient GEMM (low-order term)");
-    }
-  }
+  BwdPipeParams p{};
+  p.N = static_cast<int>(N);
+  p.V = static_cast<int>(V);
+  p.d_s = static_cast<int>(d_s);
+  p.kb_s = static_cast<int>(cdiv(d_s, kBK));
+  p.kb_t = static_cast<int>(cdiv(d_t, kBK));
+  p.ntd = static_cast<int>(ntd);
+  p.R = static_cast<int>(R);
+  p.bw = static_cast<int>(bw);
+  p.TB = static_cast<int>(TB);
+  p.VB = static_cast<int>(VB);
+  p.B = static_cast<int>(TB * VB);
+  p.c = 1.4426950408889634f / tau;
+  p.gscale = static_cast<float>(static_cast<double>(grad_scale) / (static_cast<double>(tau) * N));
+  p.lse_s = lse_s;
+  p.lse_t = lse_t;
+  p.lse_gap = lse_gap;
+  p.split = split ? 1 : 0;
+  p.ctrl = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + g_total);
+  p.ctl = WaitCtl{dev->status, wait_limit_ns()};
+  cudaError_t e = cudaMemsetAsync(p.ctrl, 0, kPipeCtrlWords * sizeof(unsigned), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clear the backward's work counters");
+  const int clusters = static_cast<int>(items < dev->pipe_clusters ? items : dev->pipe_clusters);
+  e = launch_bwd_pipe(maps, p, clusters, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "launch pipelined backward");
   return HYLO_OK;
 }
 
@@ -545,8 +518,10 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
 constexpr size_t kNoAllocFloats = kNoAllocScratchBytes / sizeof(float);
-// Largest N whose statistics fit with one vocabulary segment: 16 MiB / (6 fields * 4 B).
-constexpr int64_t kNoAllocMaxTokens = static_cast<int64_t>(kNoAllocFloats / kStatFields);
+// The last kProgressBytes hold the pacing counters; the statistics get the rest.
+constexpr size_t kNoAllocStatFloats = (kNoAllocScratchBytes - kProgressBytes) / sizeof(float);
+// Largest N whose statistics fit with one vocabulary segment: (16 MiB - 1280 B) / (6 fields * 4 B).
+constexpr int64_t kNoAllocMaxTokens = static_cast<int64_t>(kNoAllocStatFloats / kStatFields);
 
 // Every device that loads this library holds this array until the process exits.
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
@@ -614,19 +589,23 @@ extern "C" hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16
   p.token_tiles = static_cast<int>(cdiv(N, 2 * kBM));
   p.vtiles = static_cast<int>(cdiv(V, fused_bn()));
   // as many vocabulary segments as the heuristic wants, but no more than the scratch holds
-  const int64_t fit = static_cast<int64_t>(kNoAllocFloats) / (static_cast<int64_t>(kStatFields) * N);
+  const int64_t fit = static_cast<int64_t>(kNoAllocStatFloats) / (static_cast<int64_t>(kStatFields) * N);
   const int want = choose_segments(p.token_tiles, p.vtiles, dev->fused_clusters);
   p.nseg = static_cast<int>(want < fit ? want : fit);
   p.units = p.token_tiles * p.nseg;
-  p.group = 1;  // tile-major: measured least DRAM traffic for the forward (see raster_group)
+  p.group = 1;  // tile-major, as in hylo_kl_forward
   p.c = 1.4426950408889634f / tau;
   p.inv_tau = 1.0f / tau;
   p.part = scratch;  // every (segment, token) slot read by the combine step is written first
-  p.progress = nullptr;  // no pacing: the built-in scratch holds the statistics only
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
   const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
+  if (pace_launch(p.units, grid)) {  // counters at the scratch's tail; epoch-tagged, never cleared
+    p.progress = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(scratch) + kNoAllocScratchBytes -
+                                                       kProgressBytes);
+    p.epoch = next_epoch(dev);
+  }
 
-  cudaError_t e = launch_fused(fused_bn(), false, m_hs, m_Ws, m_ht, m_Wt, m_hs, m_hs, p, grid, stream);
+  cudaError_t e = launch_fused(fused_bn(), m_hs, m_Ws, m_ht, m_Wt, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
   e = launch_combine(p.part, p.N, p.nseg, p.inv_tau, kl, lse_s, lse_t, lse_gap, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch combine");

@@ -1,13 +1,10 @@
-// Fused hidden-state KL on sm_103a: one persistent, warp-specialised kernel that computes
-// the teacher and student logit tiles z_t = h_t W_t^T and z_s = h_s W_s^T on the tensor cores
-// (tcgen05 UMMA, TMA-fed 128-byte-swizzled operands, fp32 accumulators in TMEM) and consumes
-// them in the epilogue without writing logits to memory.
-//
-//   forward : folds each tile into running per-token softmax/KL statistics (online softmax
-//             rescaled by the running max) and writes one set of partial statistics per
-//             (token, vocabulary segment); a small combine kernel merges the segments.
-//   backward: recomputes the tiles, forms G = grad_scale (p_s - p_t) / (tau N) from the saved
-//             log-sum-exps and writes G in bf16 for the gradient GEMMs.
+// Fused hidden-state KL forward on sm_103a: one persistent, warp-specialised kernel that
+// computes the teacher and student logit tiles z_t = h_t W_t^T and z_s = h_s W_s^T on the tensor
+// cores (tcgen05 UMMA, TMA-fed 128-byte-swizzled operands, fp32 accumulators in TMEM) and folds
+// them in the epilogue into running per-token softmax/KL statistics (online softmax rescaled by
+// the running max), without writing logits to memory. It writes one set of partial statistics
+// per (token, vocabulary segment); a small combine kernel merges the segments. (The backward,
+// which recomputes the same tiles, is kl_bwd_pipe.cu.)
 //
 // The operation is the Stage-II distillation loss of the HyLo pages: the "Fused Hidden-State
 // KL" that skips the teacher LM head and fuses softmax+KL (Long-Context Aware Upcycling
@@ -39,7 +36,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;  // + TMA warp + UMMA warp
 // tiles. kFusedBN = 256: one (teacher, student) pair fills the 512 TMEM columns and is drained
 // between tiles. (BN = 128 would fit two pairs and overlap the epilogue with the next tile's
 // UMMAs, but N = 128 UMMAs measured 22% slower end to end on GB300, on one CTA or on a pair.)
-template <int BN_, bool BWD>
+template <int BN_>
 struct FusedCfg {
   static constexpr int BN = BN_;         // vocabulary columns per pair tile
   static constexpr int HB = BN / 2;      // W rows staged per CTA
@@ -49,9 +46,8 @@ struct FusedCfg {
   static constexpr int B_BYTES = HB * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
-  // backward: one staging buffer of 32 rows x 64 bf16 (128 B rows) per epilogue warp;
-  // forward: the statistics of one column half handed to the other half at a unit's end
-  static constexpr int EXTRA_BYTES = BWD ? kEpiWarps * 32 * 128 : kStatFields * kBM * 4;
+  // the statistics of one column half handed to the other half at a unit's end
+  static constexpr int EXTRA_BYTES = kStatFields * kBM * 4;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES + EXTRA_BYTES;
   // full[S], empty[S], tfull[NBUF], tempty[NBUF], merge_full, merge_empty, drain
   static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 3;
@@ -79,9 +75,12 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsig
 // kernel) sets the switch in slot kMaxClusters and from then on no producer of the launch
 // paces, so a late peer costs at most one such wait, never correctness.
 // (Measured: DRAM reads of the 64K forward ~250 -> ~70 GB, 3-7% less time per kernel.)
+// Every word carries the launch's 16-bit epoch in its top bits, so the counters need no
+// clearing between launches: a word from an earlier launch reads as "not started yet", and the
+// switch is on only while it holds this launch's epoch. Low 48 bits: (k << 24) | tile.
 constexpr unsigned long long kPaceLead = 2;
 constexpr unsigned long long kPaceWaitNs = 200000ull;
-constexpr unsigned long long kPaceDone = ~0ull;
+constexpr unsigned long long kPaceLow = (1ull << 48) - 1;  // low-bits value meaning "no more units"
 
 // Work unit u = (256-token pair tile, vocabulary segment); row0 = the pair tile's first token.
 __device__ __forceinline__ void unit_range(const FusedParams& p, int u, int& row0, int& vt0, int& vt1, int& seg) {
@@ -102,13 +101,12 @@ __device__ __forceinline__ void unit_range(const FusedParams& p, int u, int& row
   vt1 = static_cast<int>((static_cast<long long>(seg + 1) * p.vtiles) / p.nseg);
 }
 
-template <int BN_, bool BWD>
+template <int BN_>
 __global__ void __launch_bounds__(kThreads, 1)
 fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant__ CUtensorMap tm_Ws,
                 const __grid_constant__ CUtensorMap tm_ht, const __grid_constant__ CUtensorMap tm_Wt,
-                const __grid_constant__ CUtensorMap tm_G, const __grid_constant__ CUtensorMap tm_G2,
                 const FusedParams p) {
-  using C = FusedCfg<BN_, BWD>;
+  using C = FusedCfg<BN_>;
   constexpr int BN = C::BN;
   constexpr int HB = C::HB;
   constexpr int HALF = C::HALF;
@@ -152,8 +150,6 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
     prefetch_tmap(&tm_Ws);
     prefetch_tmap(&tm_ht);
     prefetch_tmap(&tm_Wt);
-    if (BWD) prefetch_tmap(&tm_G);
-    if (BWD && p.split) prefetch_tmap(&tm_G2);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, 512);
@@ -163,6 +159,10 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
   __syncthreads();
   cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA signal
   tc_fence_after();
+  // Everything above touched only this CTA's own resources; from here on global memory (the
+  // pacing counters, the statistics) may be shared with the previous kernel in the stream.
+  grid_dep_wait();
+  grid_dep_launch();
   const uint32_t tmem_base = *tmem_slot;
   const int kbt = p.kb_t, kbtot = p.kb_t + p.kb_s;
   const int my_rows = static_cast<int>(rank) * kBM;  // this CTA's token rows inside a pair tile
@@ -179,6 +179,7 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
         unit_range(p, u, row0, vt0, vt1, seg);
         const int arow = row0 + my_rows;
         const bool pace = p.progress != nullptr && rank == 0;
+        const unsigned long long ep = static_cast<unsigned long long>(p.epoch) << 48;
         const unsigned long long kunit = static_cast<unsigned long long>((u - cid) / ncl);
         uint32_t peers[kMaxClusters / 32] = {};  // bit j: cluster j's unit at index kunit is on this segment
         if (pace) {
@@ -194,22 +195,25 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
           const int brow = vt * BN + static_cast<int>(rank) * HB;
           if (pace) {
             volatile unsigned long long* prog = p.progress;
-            const unsigned long long mine = (kunit << 32) | static_cast<unsigned long long>(vt - vt0);
-            prog[cid] = mine;
+            const unsigned long long mine = (kunit << 24) | static_cast<unsigned long long>(vt - vt0);
+            prog[cid] = ep | mine;
             const uint64_t t0 = globaltimer_ns();
-            bool off = prog[kMaxClusters] != 0ull;
+            bool off = prog[kMaxClusters] == ep;
             for (int w = 0; !off && w < kMaxClusters / 32; ++w) {
               for (uint32_t bits = peers[w]; !off && bits != 0u; bits &= bits - 1u) {
                 const int j = 32 * w + __ffs(static_cast<int>(bits)) - 1;
                 while (true) {
                   const unsigned long long v = prog[j];
-                  if (v == kPaceDone || v + kPaceLead >= mine) break;
+                  if ((v & ~kPaceLow) == ep) {  // the peer has started this launch
+                    const unsigned long long lo = v & kPaceLow;
+                    if (lo == kPaceLow || lo + kPaceLead >= mine) break;
+                  }
                   if (globaltimer_ns() - t0 > kPaceWaitNs) {  // give up pacing for the whole launch
-                    prog[kMaxClusters] = 1ull;
+                    prog[kMaxClusters] = ep;
                     off = true;
                     break;
                   }
-                  if (prog[kMaxClusters] != 0ull) {
+                  if (prog[kMaxClusters] == ep) {
                     off = true;
                     break;
                   }
@@ -244,8 +248,9 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
           }
         }
       }
-      if (p.progress != nullptr && rank == 0)
-        *reinterpret_cast<volatile unsigned long long*>(p.progress + cid) = kPaceDone;  // no more units
+      if (p.progress != nullptr && rank == 0)  // no more units
+        *reinterpret_cast<volatile unsigned long long*>(p.progress + cid) =
+            (static_cast<unsigned long long>(p.epoch) << 48) | kPaceLow;
       if (!ok) {
         // Let every armed load land before the CTA can exit: the latest armed phase of stage s
         // has parity `phase` for stages below the current one and `phase ^ 1` otherwise.
@@ -317,7 +322,6 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
     const int row = q * 32 + lane;  // token row inside this CTA's 128 rows
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * HALF);
     float* merge = reinterpret_cast<float*>(extra);  // [kStatFields][128]
-    uint8_t* staging = extra + e * 4096;             // backward: 32 rows x 128 B
     int lt = 0, lu = 0;
     bool ok = true;
     for (int u = cid; ok && u < p.units; u += ncl, ++lu) {
@@ -325,13 +329,6 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
       unit_range(p, u, row0, vt0, vt1, seg);
       const int token = row0 + my_rows + row;
       RowStats rs{-INFINITY, 0.f, -INFINITY, 0.f, 0.f, 0.f, false};
-      float bt = 0.f, bs = 0.f, ngl = 0.f;
-      if (BWD && token < p.N) {
-        const float lt_ = p.lse_t[token], ls_ = p.lse_s[token];
-        bt = lt_ * kLog2e;
-        bs = ls_ * kLog2e;
-        ngl = -(p.lse_gap != nullptr ? p.lse_gap[token] : ls_ - lt_) * kLog2e;
-      }
       for (int vt = vt0; vt < vt1; ++vt, ++lt) {
         const int b = lt % NBUF;
         const uint32_t tph = static_cast<uint32_t>(lt / NBUF) & 1u;
@@ -344,74 +341,17 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
         const uint32_t tT = lane_base + static_cast<uint32_t>(b * 2 * BN);
         const uint32_t tS = tT + BN;
         const int col_base = vt * BN + h * HALF;
-        if (!BWD) {
 #pragma unroll 1
-          for (int c = 0; c < HALF / 32; ++c) {
-            float zt[32], zs[32];
-            tmem_ld32(tT + c * 32, zt);
-            tmem_ld32(tS + c * 32, zs);
-            tmem_ld_wait();
-            const int valid = min(32, p.V - (col_base + c * 32));
-            if (valid >= 32) {
-              fold_chunk<false>(rs, zt, zs, 0xffffffffu, p.c, p.inv_tau);
-            } else if (valid > 0) {
-              fold_chunk<true>(rs, zt, zs, (1u << valid) - 1u, p.c, p.inv_tau);
-            }
-          }
-        } else {
-          const uint32_t rowaddr = smem_u32(staging) + lane * 128;
-#pragma unroll 1
-          for (int c2 = 0; c2 < HALF / 64; ++c2) {
-            uint32_t pk[2][16], pl[2][16];  // G in bf16 and, split, its bf16 rounding remainder
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const int c = c2 * 2 + half;
-              float zt[32], zs[32];
-              tmem_ld32(tT + c * 32, zt);
-              tmem_ld32(tS + c * 32, zs);
-              tmem_ld_wait();
-              const float2 c2v = make_float2(p.c, p.c), gs2 = make_float2(p.gscale, p.gscale);
-              const float2 nbt = make_float2(-bt, -bt), nbs = make_float2(-bs, -bs), ngl2 = make_float2(ngl, ngl);
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float2 g = __fmul2_rn(prob_diff2(make_float2(zt[2 * j], zt[2 * j + 1]),
-                                                       make_float2(zs[2 * j], zs[2 * j + 1]), c2v, nbt, nbs, ngl2),
-                                            gs2);
-                const uint32_t hi = pack_bf16x2(g.x, g.y);
-                pk[half][j] = hi;
-                pl[half][j] = pack_bf16x2(g.x - __uint_as_float(hi << 16), g.y - __uint_as_float(hi & 0xffff0000u));
-              }
-            }
-            if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
-            __syncwarp();
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              const uint32_t chunk = static_cast<uint32_t>(c4 ^ (lane & 7));
-              const uint32_t* src = &pk[c4 >> 2][4 * (c4 & 3)];
-              st_shared_v4(rowaddr + chunk * 16, src[0], src[1], src[2], src[3]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && row0 + my_rows < p.N) {
-              tma_store_2d(&tm_G, staging, col_base + c2 * 64, row0 + my_rows + q * 32);
-              bulk_commit_group();
-            }
-            if (p.split) {  // the remainder through the same staging rows, once the store has read them
-              if (lane == 0) bulk_wait_group_read<0>();
-              __syncwarp();
-#pragma unroll
-              for (int c4 = 0; c4 < 8; ++c4) {
-                const uint32_t chunk = static_cast<uint32_t>(c4 ^ (lane & 7));
-                const uint32_t* src = &pl[c4 >> 2][4 * (c4 & 3)];
-                st_shared_v4(rowaddr + chunk * 16, src[0], src[1], src[2], src[3]);
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0 && row0 + my_rows < p.N) {
-                tma_store_2d(&tm_G2, staging, col_base + c2 * 64, row0 + my_rows + q * 32);
-                bulk_commit_group();
-              }
-            }
+        for (int c = 0; c < HALF / 32; ++c) {
+          float zt[32], zs[32];
+          tmem_ld32(tT + c * 32, zt);
+          tmem_ld32(tS + c * 32, zs);
+          tmem_ld_wait();
+          const int valid = min(32, p.V - (col_base + c * 32));
+          if (valid >= 32) {
+            fold_chunk<false>(rs, zt, zs, 0xffffffffu, p.c, p.inv_tau);
+          } else if (valid > 0) {
+            fold_chunk<true>(rs, zt, zs, (1u << valid) - 1u, p.c, p.inv_tau);
           }
         }
         tc_fence_before();
@@ -419,44 +359,41 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + b), 0));
       }
       if (!ok) break;
-      if (!BWD) {
-        // column half 1 hands its statistics to half 0, which merges and writes them
-        const uint32_t par = static_cast<uint32_t>(lu & 1);
-        if (h == 1) {
-          bool w = wait_bounded(merge_empty, par ^ 1u, abort_flag, p.ctl, 5);
-          if (!__all_sync(0xffffffffu, w)) break;
-          merge[0 * kBM + row] = rs.mt;
-          merge[1 * kBM + row] = rs.st;
-          merge[2 * kBM + row] = rs.ms;
-          merge[3 * kBM + row] = rs.ss;
-          merge[4 * kBM + row] = rs.a;
-          merge[5 * kBM + row] = rs.far ? -1.f : rs.cc;  // cc >= 0 otherwise, so -1 marks "far"
-          __syncwarp();
-          if (lane == 0) mbar_arrive(merge_full);
-        } else {
-          bool w = wait_bounded(merge_full, par, abort_flag, p.ctl, 6);
-          if (!__all_sync(0xffffffffu, w)) break;
-          const float occ = merge[5 * kBM + row];
-          const RowStats o{merge[0 * kBM + row], merge[1 * kBM + row], merge[2 * kBM + row],
-                           merge[3 * kBM + row], merge[4 * kBM + row], occ < 0.f ? 0.f : occ, occ < 0.f};
-          __syncwarp();
-          if (lane == 0) mbar_arrive(merge_empty);
-          merge_stats(rs, o, p.c);
-          if (token < p.N) {
-            const size_t NS = static_cast<size_t>(p.N);
-            float* base = p.part + static_cast<size_t>(seg) * NS + token;
-            const size_t fs = static_cast<size_t>(p.nseg) * NS;  // stride between fields
-            base[0 * fs] = rs.mt;
-            base[1 * fs] = rs.st;
-            base[2 * fs] = rs.ms;
-            base[3 * fs] = rs.ss;
-            base[4 * fs] = rs.a;
-            base[5 * fs] = rs.far ? -1.f : rs.cc;
-          }
+      // column half 1 hands its statistics to half 0, which merges and writes them
+      const uint32_t par = static_cast<uint32_t>(lu & 1);
+      if (h == 1) {
+        bool w = wait_bounded(merge_empty, par ^ 1u, abort_flag, p.ctl, 5);
+        if (!__all_sync(0xffffffffu, w)) break;
+        merge[0 * kBM + row] = rs.mt;
+        merge[1 * kBM + row] = rs.st;
+        merge[2 * kBM + row] = rs.ms;
+        merge[3 * kBM + row] = rs.ss;
+        merge[4 * kBM + row] = rs.a;
+        merge[5 * kBM + row] = rs.far ? -1.f : rs.cc;  // cc >= 0 otherwise, so -1 marks "far"
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merge_full);
+      } else {
+        bool w = wait_bounded(merge_full, par, abort_flag, p.ctl, 6);
+        if (!__all_sync(0xffffffffu, w)) break;
+        const float occ = merge[5 * kBM + row];
+        const RowStats o{merge[0 * kBM + row], merge[1 * kBM + row], merge[2 * kBM + row],
+                         merge[3 * kBM + row], merge[4 * kBM + row], occ < 0.f ? 0.f : occ, occ < 0.f};
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merge_empty);
+        merge_stats(rs, o, p.c);
+        if (token < p.N) {
+          const size_t NS = static_cast<size_t>(p.N);
+          float* base = p.part + static_cast<size_t>(seg) * NS + token;
+          const size_t fs = static_cast<size_t>(p.nseg) * NS;  // stride between fields
+          base[0 * fs] = rs.mt;
+          base[1 * fs] = rs.st;
+          base[2 * fs] = rs.ms;
+          base[3 * fs] = rs.ss;
+          base[4 * fs] = rs.a;
+          base[5 * fs] = rs.far ? -1.f : rs.cc;
         }
       }
     }
-    if (BWD && lane == 0) bulk_wait_group<0>();
   }
 
   tc_fence_before();
@@ -523,42 +460,38 @@ __global__ void __launch_bounds__(1024) kl_mean_kernel(const float* __restrict__
   if (threadIdx.x == 0) loss[0] = static_cast<float>(red[0] / static_cast<double>(N));
 }
 
-template <int BN, bool BWD>
+// attr must hold two entries: the cluster shape and programmatic stream serialization (the
+// kernel may start while its predecessor finishes; see grid_dep_wait()).
+template <int BN>
 cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, int clusters, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = FusedCfg<BN, BWD>::SMEM;
+  cfg.dynamicSmemBytes = FusedCfg<BN>::SMEM;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cfg;
 }
 
-template <int BN, bool BWD>
+template <int BN>
 cudaError_t prepare_one(int* max_clusters) {
-  cudaError_t e = cudaFuncSetAttribute(fused_kl_kernel<BN, BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       FusedCfg<BN, BWD>::SMEM);
+  cudaError_t e =
+      cudaFuncSetAttribute(fused_kl_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, FusedCfg<BN>::SMEM);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config<BN, BWD>(attr, 1, nullptr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_config<BN>(attr, 1, nullptr);
+  cfg.numAttrs = 1;  // occupancy: the cluster shape only
   int n = 0;
-  if ((e = cudaOccupancyMaxActiveClusters(&n, fused_kl_kernel<BN, BWD>, &cfg)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveClusters(&n, fused_kl_kernel<BN>, &cfg)) != cudaSuccess) return e;
   if (n < *max_clusters) *max_clusters = n;
   return cudaSuccess;
-}
-
-template <int BN, bool BWD>
-cudaError_t launch_one(const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht, const CUtensorMap& Wt,
-                       const CUtensorMap& G, const CUtensorMap& G2, const FusedParams& p, int clusters,
-                       cudaStream_t stream) {
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config<BN, BWD>(attr, clusters, stream);
-  return cudaLaunchKernelEx(&cfg, fused_kl_kernel<BN, BWD>, hs, Ws, ht, Wt, G, G2, p);
 }
 
 }  // namespace
@@ -566,17 +499,15 @@ cudaError_t launch_one(const CUtensorMap& hs, const CUtensorMap& Ws, const CUten
 cudaError_t fused_prepare(int bn, int* max_clusters) {
   if (bn != kFusedBN) return cudaErrorInvalidValue;
   *max_clusters = 1 << 30;
-  cudaError_t e;
-  if ((e = prepare_one<kFusedBN, false>(max_clusters)) != cudaSuccess) return e;
-  return prepare_one<kFusedBN, true>(max_clusters);
+  return prepare_one<kFusedBN>(max_clusters);
 }
 
-cudaError_t launch_fused(int bn, bool backward, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
-                         const CUtensorMap& Wt, const CUtensorMap& G, const CUtensorMap& G2, const FusedParams& p,
-                         int clusters, cudaStream_t stream) {
+cudaError_t launch_fused(int bn, const CUtensorMap& hs, const CUtensorMap& Ws, const CUtensorMap& ht,
+                         const CUtensorMap& Wt, const FusedParams& p, int clusters, cudaStream_t stream) {
   if (bn != kFusedBN) return cudaErrorInvalidValue;
-  return backward ? launch_one<kFusedBN, true>(hs, Ws, ht, Wt, G, G2, p, clusters, stream)
-                  : launch_one<kFusedBN, false>(hs, Ws, ht, Wt, G, G2, p, clusters, stream);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_config<kFusedBN>(attr, clusters, stream);
+  return cudaLaunchKernelEx(&cfg, fused_kl_kernel<kFusedBN>, hs, Ws, ht, Wt, p);
 }
 
 cudaError_t launch_combine(const float* part, int N, int nseg, float inv_tau, float* kl, float* lse_s,

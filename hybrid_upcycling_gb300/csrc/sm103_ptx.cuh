@@ -49,6 +49,15 @@ __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(N));
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization may
+// start while its predecessor in the stream is still finishing; grid_dep_wait() blocks until
+// the predecessor grid has completed and its memory operations are visible, so it must come
+// before the first global-memory access that could depend on (or conflict with) the
+// predecessor. grid_dep_launch() lets the successor's CTAs be scheduled as SMs free up.
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
@@ -157,6 +166,23 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* s
                :: "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1) : "memory");
 }
 
+// 3-D tiled load into this CTA's shared memory, completion counted on an mbarrier that may live
+// in the peer CTA of the pair (cluster address). c0 innermost.
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* m, uint32_t mbar_cluster,
+                                                 int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+      :: "r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(mbar_cluster), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// 3-D tiled store shared -> global (elements outside the tensor are not written).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* smem_src, int32_t c0, int32_t c1,
+                                             int32_t c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+               :: "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
 // 2-D tiled reduce-add shared -> global (fp32 add into the existing values).
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, const void* smem_src, int32_t c0, int32_t c1) {
   asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
@@ -173,6 +199,37 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 template <int N>
 __device__ __forceinline__ void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" :: "n"(N) : "memory");
+}
+
+// Orders this thread's earlier async-proxy (TMA) accesses of global memory before its later
+// generic-proxy accesses, and vice versa.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ------------------------------------------------------------ counters shared between CTAs
+// Release-add to a counter in global memory (gpu scope): memory operations ordered before it
+// (in this thread, or made visible to it through a CTA barrier) are visible to any thread that
+// reads the new value with ld_acquire_gpu.
+__device__ __forceinline__ void red_release_gpu_add(unsigned* ctr, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(ctr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* ctr) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+  return v;
+}
+
+// Release store / acquire load of a word in this CTA's shared memory.
+__device__ __forceinline__ void st_release_cta_shared(uint32_t* addr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" :: "r"(smem_u32(addr)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_cta_shared(const uint32_t* addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(addr)) : "memory");
+  return v;
 }
 
 // ------------------------------------------------------------------------------- tcgen05

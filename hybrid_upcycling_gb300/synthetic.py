@@ -63,6 +63,10 @@ class Workload:
     def flops_fwd(self) -> float:
         return 2.0 * self.N * self.V * (self.d_s + self.d_t)
 
+    def flops_bwd(self) -> float:
+        """Backward: the logit recompute 2 N V (d_s + d_t) plus dh_s and dW_s, 4 N V d_s."""
+        return 2.0 * self.N * self.V * (3 * self.d_s + self.d_t)
+
     def with_sizes(self, **kw) -> "Workload":
         return replace(self, **kw)
 

@@ -57,11 +57,12 @@ typedef enum {
   HYLO_ERR_ARCH = -8       /* the current device is not sm_103 */
 } hylo_status;
 
-/* Bytes of device workspace that hylo_kl_forward and hylo_kl_backward need for these sizes.
- * It is O(N) for the forward (per-token partial softmax statistics) and
- * O(token_chunk * V) bf16 for the backward (the gradient of one token chunk's logits),
- * never O(N * V), plus 1.25 KB of counters with which the fused kernels keep the clusters that
- * share LM-head tiles in step (cleared by each call). Returns 0 for invalid sizes.
+/* Bytes of device workspace that hylo_kl_forward and hylo_kl_backward need for these sizes:
+ * the larger of the forward's per-token partial softmax statistics (6 x 32 x N fp32, O(N)) and
+ * the backward's staging of G = dL/dz_s for one block of tokens x vocabulary words (bf16, at
+ * most 64 MiB whatever N, V and token_chunk), plus 1280 bytes of counters with which the fused
+ * kernels keep the clusters that share LM-head tiles in step. So the extra memory is
+ * O(N) + 64 MiB, never O(N * V) or O(token_chunk * V). Returns 0 for invalid sizes.
  * token_chunk <= 0 means 4096. */
 size_t hylo_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
                                int64_t token_chunk);
@@ -84,9 +85,10 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s,
 
 /* Backward: dh_s [N, d_s] and dW_s [V, d_s] (fp32, OVERWRITTEN, not accumulated) for
  * grad_scale * loss, from the lse_s / lse_t (and lse_gap, if not NULL) that hylo_kl_forward
- * wrote for the same inputs. Per token chunk it recomputes both logit tiles, forms G in bf16
- * in the workspace (token_chunk x V), then runs dh_s = G W_s and dW_s += G^T h_s on the
- * tensor cores. Where p_s and p_t of a word agree to within a factor 2^(1/4), G takes the form
+ * wrote for the same inputs. It walks the tokens in blocks of min(token_chunk, N, 32768) rows
+ * and the vocabulary in blocks sized so that one block of G (bf16) fits 64 MiB of the
+ * workspace; per block it recomputes both logit tiles, forms G, then adds G W_s into dh_s and
+ * G^T h_s into dW_s on the tensor cores. Where p_s and p_t of a word agree to within a factor 2^(1/4), G takes the form
  * p_t (2^D - 1), D = log2(p_s / p_t) from the logit difference and lse_gap, which has no
  * cancellation; with lse_gap NULL the gap is lse_s - lse_t, whose rounding bounds the
  * relative accuracy of G at ~1e-6 / |p_s / p_t - 1|. Results match for any token_chunk up
@@ -106,7 +108,7 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s,
  * bf16 rounding of G leaves -- which matters where a token's gradient is dominated by one or
  * two words (near one-hot distributions, or a student that differs from its teacher on few
  * words), where one rounding alone can exceed 2e-3. Costs one more gradient GEMM per chunk
- * and twice the backward part of the workspace: pass at least
+ * and twice the backward's G staging (2 x 64 MiB at most): pass at least
  * hylo_kl_workspace_bytes_split(...) bytes. (The pages describe no such variant; it is a
  * precision option of this library.) */
 size_t hylo_kl_workspace_bytes_split(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
@@ -126,13 +128,16 @@ hylo_status hylo_kl_backward_split(const uint16_t* h_s, const uint16_t* W_s,
  * the per-token partial statistics go to a 16 MiB array built into the library, which every
  * GPU that loads the library holds until the process exits.
  *   - Same arguments, outputs and results as hylo_kl_forward, minus the workspace pair.
- *   - N may be at most 699050 (16 MiB / 24 bytes of statistics per token); larger N returns
- *     HYLO_ERR_DIM with a message. Smaller N may use fewer vocabulary segments than
- *     hylo_kl_forward would, which changes results only by fp32 summation order.
+ *   - N may be at most 698997 ((16 MiB - 1280 bytes of pacing counters) / 24 bytes of
+ *     statistics per token); larger N returns HYLO_ERR_DIM with a message. Larger N may use
+ *     fewer vocabulary segments than hylo_kl_forward would, which changes results only by fp32
+ *     summation order. Launches of several waves pace their clusters like hylo_kl_forward, with
+ *     the counters at the end of the built-in array.
  *   - The first call on each device looks up the array's device address (with that device
  *     current); make that first call before any stream capture.
  *   - All calls share the one array per device and it keeps the last call's contents (each call
- *     writes every slot it reads, so nothing needs clearing). Calls that overlap on the GPU
+ *     writes every statistics slot it reads, and the pacing counters carry the launch's tag,
+ *     so nothing needs clearing). Calls that overlap on the GPU
  *     (different streams, or threads without ordering) race on it: serialise them. */
 hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16_t* W_s,
                                     const uint16_t* h_t, const uint16_t* W_t,

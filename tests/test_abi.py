@@ -38,18 +38,42 @@ def test_exports_every_declared_symbol(lib):
 
 
 PACE = 1280  # the fused kernels' pacing counters: one 8-byte word per cluster and a switch, to 256 B
+G_RING = 64 << 20  # the backward's G staging: three blocks of tokens x words, at most 64 MiB in all
+
+
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+def _g_ring(N, V, chunk):
+    """Bytes of the G ring as documented: 3 blocks of R x bw bf16, R = token_chunk rounded up to
+    256 (at most 32768, at most N rounded up), bw = 64 MiB / (6 R) rounded down to 256 words (at
+    most V rounded up)."""
+    c = 4096 if chunk <= 0 else min(chunk, 32768)
+    R = min(_r256(c), _r256(N))
+    bw = min((G_RING // (6 * R)) // 256 * 256, _r256(V))
+    return 3 * R * bw * 2
 
 
 def test_workspace_bytes(lib):
+    """O(N) statistics for the forward, a G ring of at most 64 MiB for the backward: the size
+    is bounded independently of V x token_chunk (and never N x V)."""
     N, d_s, d_t, V = 65536, 2048, 4096, 128256
     fwd = 6 * 32 * N * 4
-    bwd = 4096 * V * 2
-    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096) == max(fwd, bwd) + PACE
-    # O(N + token_chunk * V), never N * V
-    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 1024) == max(fwd, 1024 * V * 2) + PACE
-    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096) < N * V * 2 // 8
-    # chunk larger than N is clamped to N; <= 0 means 4096
-    assert _lib.hylo_kl_workspace_bytes(100, 64, 128, 513, 100000) == max(6 * 32 * 100 * 4, ((100 * 520 * 2 + 255) // 256) * 256) + PACE
+    # 3 blocks of 4096 tokens x 2560 words of bf16 G = 60 MiB
+    assert _g_ring(N, V, 4096) == 60 << 20
+    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096) == max(fwd, 60 << 20) + PACE
+    for n, v, chunk in ((65536, 128256, 4096), (65536, 151936, 1024), (4096, 128256, 4096), (1000, 262144, 4096),
+                        (100000, 128256, 100000), (65536, 128256, 65536), (8192, 1 << 20, 8192), (300, 1000, 7),
+                        (100, 513, 100000), (64, 100, 4096), (1, 3, 0)):
+        ws = _lib.hylo_kl_workspace_bytes(n, d_s, d_t, v, chunk)
+        assert ws == max(_r256(6 * 32 * n * 4), _r256(_g_ring(n, v, chunk))) + PACE, (n, v, chunk)
+        assert ws <= max(6 * 32 * n * 4, G_RING) + PACE, (n, v, chunk, ws)
+        wss = _lib.hylo_kl_workspace_bytes_split(n, d_s, d_t, v, chunk)
+        assert wss == max(_r256(6 * 32 * n * 4), 2 * _r256(_g_ring(n, v, chunk))) + PACE
+        assert wss <= max(6 * 32 * n * 4, 2 * G_RING) + PACE
+    # at N <= 4096 tokens (one token block) the G staging is still at most 64 MiB, not N x V
+    assert _lib.hylo_kl_workspace_bytes(4096, d_s, d_t, V, 4096) < 4096 * V * 2
     assert _lib.hylo_kl_workspace_bytes(8192, 64, 64, 1000, 0) == _lib.hylo_kl_workspace_bytes(8192, 64, 64, 1000, 4096)
     # invalid sizes give 0
     assert _lib.hylo_kl_workspace_bytes(0, 64, 64, 10, 4096) == 0
@@ -145,10 +169,7 @@ def test_split_workspace_and_rejection(lib):
     N, d_s, d_t, V = 8192, 2048, 4096, 128256
     one = _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096)
     two = _lib.hylo_kl_workspace_bytes_split(N, d_s, d_t, V, 4096)
-    g = ((4096 * V * 2 + 255) // 256) * 256
-    assert one == g + PACE and two == 2 * g + PACE
-    # few tokens: the forward's O(N) statistics dominate both
-    assert _lib.hylo_kl_workspace_bytes_split(64, 64, 64, 100, 4096) == 6 * 32 * 64 * 4 + PACE
+    assert one == (60 << 20) + PACE and two == (120 << 20) + PACE
     a = dict(h_s=FAKE, W_s=FAKE, h_t=FAKE, W_t=FAKE, N=16, d_s=64, d_t=128, V=100, tau=1.0, chunk=4096,
              lse_s=FAKE, lse_t=FAKE, gap=None, gs=1.0, dh=FAKE, dW=FAKE, ws=FAKE, stream=None)
     small = _lib.hylo_kl_workspace_bytes(4096, 64, 128, 100000, 4096)

@@ -265,9 +265,12 @@ def test_token_chunk_invariance_and_determinism():
     c = run(x, 1.0, token_chunk=4096)
     for k in ("kl", "lse_s", "lse_t", "loss", "dh", "dW"):
         assert torch.equal(a[k], c[k]), k  # bit-identical reruns
-    for k in ("kl", "lse_s", "lse_t", "loss", "dh"):
-        assert torch.equal(a[k], b[k]), k  # per-token results do not depend on the chunk
-    assert frob_rel(f64(b["dW"]), f64(a["dW"])) < 1e-6  # dW differs only by fp32 summation order
+    for k in ("kl", "lse_s", "lse_t", "loss"):
+        assert torch.equal(a[k], b[k]), k  # the forward does not depend on the chunk
+    # the gradients differ only by fp32 summation order (the token and vocabulary blocks over
+    # which dh_s and dW_s are accumulated depend on the chunk)
+    assert frob_rel(f64(b["dh"]), f64(a["dh"])) < 1e-6
+    assert frob_rel(f64(b["dW"]), f64(a["dW"])) < 1e-6
 
 
 def test_runs_on_a_side_stream():
@@ -303,7 +306,8 @@ def test_same_results_beside_a_concurrent_kernel():
 def test_library_allocates_no_device_memory():
     """The caller owns every byte: after a first call on the device (one-time set-up), a
     forward + backward leaves the device's free memory unchanged, so the peak extra memory is
-    the workspace the caller passed -- O(N + token_chunk V), not the O(N V) of dense logits."""
+    the workspace the caller passed -- O(N) statistics or one G block of at most 64 MiB, not
+    the O(N V) of dense logits."""
     N, d_s, d_t, V, chunk = 1000, 128, 256, 5000, 512
     x = gen(N, d_s, d_t, V, seed=12)
     ws = torch.empty(_lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, chunk), dtype=torch.uint8, device="cuda")
@@ -324,9 +328,9 @@ def test_library_allocates_no_device_memory():
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0, (free0, free1)
-    # O(N) statistics or one chunk's bf16 G, whichever is larger (+ 1 KB of pacing counters);
-    # below one model's fp32 logits
-    assert ws.numel() <= max(6 * 32 * N * 4, chunk * ((V + 7) // 8 * 8) * 2) + 256 + 1280
+    # O(N) statistics or the G ring of at most 64 MiB, whichever is larger (+ 1280 B of
+    # counters); below one model's fp32 logits
+    assert ws.numel() <= max(6 * 32 * N * 4, 64 << 20) + 1280
     assert ws.numel() < 4 * N * V
 
 

@@ -24,7 +24,7 @@ def test_noalloc_rejects_bad_arguments_without_touching_the_gpu():
     lib = _lib.load()
     assert _noalloc(lib, ptr=None) == -1
     assert _noalloc(lib, d_s=12) == -2
-    assert _noalloc(lib, N=699051) == -2  # more tokens than the built-in scratch holds
+    assert _noalloc(lib, N=698998) == -2  # more tokens than the built-in scratch holds
     assert b"built-in scratch" in lib.hylo_kl_last_error()
     assert _noalloc(lib, ptr=FAKE + 4) == -3
     assert _noalloc(lib, tau=0.0) == -4
