@@ -89,7 +89,8 @@ constexpr int kPipeCtrlWords = 2 + kGRing;
 // fit on the device at once.
 cudaError_t bwd_pipe_prepare(int* max_clusters);
 // Maps: hs, ht, Ws, Wt K-major (box 64 x 128); WsB, hsB MN-major (box 64 x 64); dh, dW fp32
-// (box 32 x 32); G, GA, GT over the ring [slots][R][bw] bf16 (boxes 64 x 32, 64 x 128, 64 x 64).
+// (box 32 x 32); G, GA, GT over the ring [slots][R][bw] bf16 (boxes 32 x 32 with 64-byte
+// swizzle, 64 x 128, 64 x 64).
 cudaError_t launch_bwd_pipe(const CUtensorMap* maps, const BwdPipeParams& p, int clusters, cudaStream_t stream);
 constexpr int kPipeMaps = 11;
 

@@ -134,16 +134,17 @@ unsigned next_epoch(DeviceState* d) {
   return d->pace_epoch;
 }
 
-// 3-D tensor map [outer2][outer1][inner] (contiguous), 128-byte swizzle, zero fill outside.
+// 3-D tensor map [outer2][outer1][inner] (contiguous), zero fill outside; 128-byte swizzle
+// unless `swizzle` says otherwise.
 hylo_status make_map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner, uint64_t outer1,
-                        uint64_t outer2, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer1) {
+                        uint64_t outer2, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer1,
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   cuuint64_t dims[3] = {inner, outer1, outer2};
   cuuint64_t strides[2] = {row_bytes, row_bytes * outer1};
   cuuint32_t box[3] = {box_inner, box_outer1, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(HYLO_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed with CUresult %d", static_cast<int>(r));
   return HYLO_OK;
 }
@@ -354,7 +355,8 @@ hylo_status backward_impl(const uint16_t* h_s, const uint16_t* W_s, const uint16
   if ((st = make_map(&maps[5], h_s, bf, d_s, N, d_s * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major B of dW
   if ((st = make_map(&maps[6], dh_s, f32, d_s, N, d_s * 4, 32, 32)) != HYLO_OK) return st;
   if ((st = make_map(&maps[7], dW_s, f32, d_s, V, d_s * 4, 32, 32)) != HYLO_OK) return st;
-  if ((st = make_map_3d(&maps[8], G, bf, bw, R, slots, bw * 2, 64, 32)) != HYLO_OK) return st;    // G tile stores
+  if ((st = make_map_3d(&maps[8], G, bf, bw, R, slots, bw * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != HYLO_OK)
+    return st;  // G tile stores (32 x 32)
   if ((st = make_map_3d(&maps[9], G, bf, bw, R, slots, bw * 2, kBK, kBM)) != HYLO_OK) return st;  // K-major A of dh
   if ((st = make_map_3d(&maps[10], G, bf, bw, R, slots, bw * 2, 64, kBK)) != HYLO_OK) return st;  // MN-major A of dW
 

@@ -28,13 +28,20 @@
 // running CTA, so the launch cannot deadlock whatever the residency; in this order the waits
 // almost never block.
 //
-// Roles (320 threads per CTA of a cluster pair): warp 0 of the even CTA takes items from the
+// Roles (384 threads per CTA of a cluster pair): warp 0 of the even CTA takes items from the
 // queue and publishes them to both CTAs through a small shared-memory item ring; warp 0 of each
 // CTA waits for the item's dependencies and issues its TMA loads; warp 1 of the even CTA issues
-// the UMMAs; warps 2..9 of both CTAs are the epilogue (lane quarter w & 3, column half
-// (w - 2) >> 2 of each 256-column accumulator). TMEM holds two 256-column halves: an F item
-// takes both (teacher, student), an M item one (alternating), so consecutive M items overlap
-// their epilogue with the next item's UMMAs.
+// the UMMAs; warps 4..11 of both CTAs are the epilogue (lane quarter w & 3, column half
+// (w - 4) >> 2 of each 256-column accumulator). Warpgroup 0 gives registers to the two epilogue
+// warpgroups (setmaxnreg: 56 and 224 per thread).
+//
+// TMEM holds two 256-column halves. An M item takes one; an F item takes one for the teacher
+// tile and the other for the student tile. The UMMA warp signals the teacher half as soon as its
+// tiles are done, and the epilogue copies all 128 teacher logits of its row into registers and
+// frees that half before the student tile is even complete; it frees the student half after
+// forming G. Halves are handed out so that the next item's UMMAs always start in the half
+// freed first (after an F item, its teacher half; after an M item, the other half), so the
+// epilogue's work overlaps the UMMAs of the next item instead of stalling them.
 #include <cmath>
 
 #include "hylo_internal.h"
@@ -44,14 +51,20 @@ namespace hylo {
 namespace {
 
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiWarp0 = 4;                      // first epilogue warp (warpgroups 1 and 2)
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kRegsControl = 56;                  // per thread, warpgroup 0 (scheduler, TMA, UMMA)
+constexpr int kRegsEpilogue = 224;                // per thread, warpgroups 1 and 2
+static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= kThreads * 168, "register split");
 constexpr int BN = 256;                           // columns of every pair tile
 constexpr int HB = BN / 2;                        // B rows staged per CTA
 constexpr int A_BYTES = kBM * kBK * 2;            // 16 KB: this CTA's 128 rows of A
 constexpr int B_BYTES = HB * kBK * 2;             // 16 KB: this CTA's 128 rows of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int STAGES = 6;
-constexpr int STAGING_BYTES = kEpiWarps * 4096;   // per epilogue warp: 32 rows x 128 B
+// per epilogue warp: 32 rows x 128 B (M items: 32 fp32 columns, 128-byte swizzle; F items: two
+// tiles of 32 rows x 32 bf16 columns, 64-byte swizzle)
+constexpr int STAGING_BYTES = kEpiWarps * 4096;
 constexpr int kItemDepth = 4;
 constexpr int ITEM_OFF = STAGES * STAGE_BYTES + STAGING_BYTES;
 constexpr int BAR_OFF = ITEM_OFF + kItemDepth * 32;
@@ -66,6 +79,7 @@ static_assert(SMEM <= 232448, "shared memory budget");
 constexpr int kItemConsumers = 2 * (1 + kEpiWarps);
 
 enum : int { kItemF = 0, kItemDW = 1, kItemDH = 2, kItemEnd = 3 };
+// kMapG: G tile stores, box 32 x 32 words with 64-byte swizzle
 enum : int { kMapHs = 0, kMapHt, kMapWs, kMapWt, kMapWsB, kMapHsB, kMapDh, kMapDW, kMapG, kMapGA, kMapGT };
 
 struct PipeMaps {
@@ -233,11 +247,13 @@ __device__ __forceinline__ uint64_t slice_desc(bool mn, uint32_t base, int k) {
 }
 
 // 64-deep k-blocks of an M item (both passes when split).
-__device__ __forceinline__ int m_kblocks(const BwdPipeParams& p, const Geo& g, int kind) {
+template <bool SPLIT>
+__device__ __forceinline__ int m_kblocks(const Geo& g, int kind) {
   const int k = kind == kItemDW ? (g.R + kBK - 1) / kBK : (g.Vb + kBK - 1) / kBK;
-  return p.split ? 2 * k : k;
+  return SPLIT ? 2 * k : k;
 }
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_pipe_kernel(const __grid_constant__ PipeMaps maps, const BwdPipeParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -293,6 +309,7 @@ bwd_pipe_kernel(const __grid_constant__ PipeMaps maps, const BwdPipeParams p) {
   const uint32_t tmem_base = *tmem_slot;
   const int kbt = p.kb_t, kbf = p.kb_t + p.kb_s;
 
+  if (warp < kEpiWarp0) setmaxnreg_dec<kRegsControl>();  // each warpgroup changes its registers at once
   if (warp == 0) {
     // ------------------------------------------- scheduler (even CTA) and TMA producer (both CTAs)
     if (lane == 0) {
@@ -332,7 +349,7 @@ bwd_pipe_kernel(const __grid_constant__ PipeMaps maps, const BwdPipeParams p) {
         }
         fence_proxy_async_global();  // the G tiles other CTAs stored are read by TMA below
         const Geo g = geo(p, it.b);
-        const int nkb = it.kind == kItemF ? kbf : m_kblocks(p, g, it.kind);
+        const int nkb = it.kind == kItemF ? kbf : m_kblocks<SPLIT>(g, it.kind);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_bounded(empty + stage, phase ^ 1u, abort_flag, p.ctl, 25)) {
             ok = false;
@@ -357,7 +374,7 @@ bwd_pipe_kernel(const __grid_constant__ PipeMaps maps, const BwdPipeParams p) {
               tma_load_2d_pair(sb, &maps.m[kMapWs], fbar, (kb - kbt) * kBK, brow);
             }
           } else {
-            const int half = p.split ? nkb / 2 : nkb;
+            const int half = SPLIT ? nkb / 2 : nkb;
             const int kk = kb < half ? kb : kb - half;
             const int z = g.slot + (kb < half ? 0 : kGRing);
             const int mi = it.idx / p.ntd, nj = it.idx - (it.idx / p.ntd) * p.ntd;
@@ -412,12 +429,14 @@ bwd_pipe_kernel(const __grid_constant__ PipeMaps maps, const BwdPipeParams p) {
         if (it.kind == kItemEnd) break;
         const Geo g = geo(p, it.b);
         if (it.kind == kItemF) {
-          // teacher tile (K = d_t) into half 0, student tile (K = d_s) into half 1; each half is
-          // awaited only before its own UMMAs, so the previous item's drain of half 1 overlaps
-          // the teacher UMMAs
+          // teacher tile (K = d_t) into half t = hp, student tile (K = d_s) into the other; each
+          // half is awaited just before its own UMMAs, and the teacher half is signalled as soon
+          // as its UMMAs are done
+          const int t = hp, sh = hp ^ 1;
           for (int kb = 0; kb < kbf; ++kb) {
             if (kb == 0 || kb == kbt) {
-              const int h = kb == 0 ? 0 : 1;
+              const int h = kb == 0 ? t : sh;
+              if (kb == kbt) umma_commit_pair(tfull + t, 0x3);
               if (!wait_bounded(tempty + h, (uses[h] & 1u) ^ 1u, abort_flag, p.ctl, 27)) {
                 ok = false;
                 break;
@@ -432,7 +451,7 @@ bwd_pipe_kernel(const __grid_constant__ PipeMaps maps, const BwdPipeParams p) {
             const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
             const uint32_t sb = sa + A_BYTES;
             const bool teacher = kb < kbt;
-            const uint32_t d = tmem_base + (teacher ? 0u : static_cast<uint32_t>(BN));
+            const uint32_t d = tmem_base + static_cast<uint32_t>((teacher ? t : sh) * BN);
             const int kk = teacher ? kb : kb - kbt;
 #pragma unroll
             for (int q = 0; q < kBK / 16; ++q) {
@@ -447,8 +466,7 @@ bwd_pipe_kernel(const __grid_constant__ PipeMaps maps, const BwdPipeParams p) {
             }
           }
           if (!ok) break;
-          umma_commit_pair(tfull + 0, 0x3);
-          umma_commit_pair(tfull + 1, 0x3);
+          umma_commit_pair(tfull + sh, 0x3);
           ++uses[0];
           ++uses[1];
         } else {
@@ -462,7 +480,7 @@ bwd_pipe_kernel(const __grid_constant__ PipeMaps maps, const BwdPipeParams p) {
           const bool amn = it.kind == kItemDW;
           const uint32_t idesc = amn ? kIdescDW : kIdescDH;
           const uint32_t d = tmem_base + static_cast<uint32_t>(h * BN);
-          const int nkb = m_kblocks(p, g, it.kind);
+          const int nkb = m_kblocks<SPLIT>(g, it.kind);
           for (int kb = 0; kb < nkb; ++kb) {
             if (!wait_bounded(full + stage, phase, abort_flag, p.ctl, 30)) {
               ok = false;
@@ -492,14 +510,17 @@ bwd_pipe_kernel(const __grid_constant__ PipeMaps maps, const BwdPipeParams p) {
         drain_wait(drain, 0, 100000000ull);
       }
     }
-  } else {
+  } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
-    const int e = warp - 2;         // 0..7
-    const int q = warp & 3;         // TMEM lane quarter this warp may access
-    const int hc = e >> 2;          // column half of a 256-column accumulator
+    setmaxnreg_inc<kRegsEpilogue>();
+    const int e = warp - kEpiWarp0;  // 0..7
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int hc = e >> 2;           // column half of a 256-column accumulator
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(hc * HB);
     uint8_t* staging = staging_all + e * 4096;
-    const uint32_t rowaddr = smem_u32(staging) + lane * 128;
+    const uint32_t rowaddr = smem_u32(staging) + lane * 128;  // M items: this lane's 128-byte row
+    const uint32_t row64 = smem_u32(staging) + lane * 64;     // F items: this lane's 64-byte row
+    const uint32_t swz64 = static_cast<uint32_t>((lane >> 1) & 3);
     const uint32_t lead_iempty = mapa_shared(smem_u32(iempty), 0);
     const uint32_t lead_tempty = mapa_shared(smem_u32(tempty), 0);
     uint32_t uses[2] = {0u, 0u};
@@ -533,65 +554,75 @@ bwd_pipe_kernel(const __grid_constant__ PipeMaps maps, const BwdPipeParams p) {
           bs = ls_ * kLog2e;
           ngl = -(p.lse_gap != nullptr ? p.lse_gap[token] : ls_ - lt_) * kLog2e;
         }
-        bool w0 = wait_bounded(tfull + 0, uses[0] & 1u, abort_flag, p.ctl, 32);
-        bool w1 = w0 && wait_bounded(tfull + 1, uses[1] & 1u, abort_flag, p.ctl, 32);
-        if (!__all_sync(0xffffffffu, w1)) break;
+        const int t = hp, sh = hp ^ 1;
+        // the teacher tile: all 128 logits of this row and column half into registers, then the
+        // half goes back to the UMMAs
+        const bool wt = wait_bounded(tfull + t, uses[t] & 1u, abort_flag, p.ctl, 32);
+        if (!__all_sync(0xffffffffu, wt)) break;
         tc_fence_after();
-        const uint32_t tT = lane_base;
-        const uint32_t tS = lane_base + static_cast<uint32_t>(BN);
+        float zt[HB];
+#pragma unroll
+        for (int c = 0; c < HB / 32; ++c) tmem_ld32_at(lane_base + static_cast<uint32_t>(t * BN + c * 32), zt + 32 * c);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(lead_tempty + t * 8);
+        const bool ws = wait_bounded(tfull + sh, uses[sh] & 1u, abort_flag, p.ctl, 32);
+        if (!__all_sync(0xffffffffu, ws)) break;
+        tc_fence_after();
+        ++uses[0];
+        ++uses[1];
         const int col_local = vi * BN + hc * HB;  // first block column of this warp
         const float2 c2v = make_float2(p.c, p.c), gs2 = make_float2(p.gscale, p.gscale);
         const float2 nbt = make_float2(-bt, -bt), nbs = make_float2(-bs, -bs), ngl2 = make_float2(ngl, ngl);
-#pragma unroll 1
-        for (int c2 = 0; c2 < HB / 64; ++c2) {
-          uint32_t pk[2][16], pl[2][16];  // G in bf16 and, split, its bf16 rounding remainder
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int c = c2 * 2 + hh;
-            float zt[32], zs[32];
-            tmem_ld32(tT + c * 32, zt);
-            tmem_ld32(tS + c * 32, zs);
-            tmem_ld_wait();
-            const int vcols = g.Vb - (col_local + c * 32);  // columns of this chunk inside the vocabulary
+        for (int c = 0; c < HB / 32; ++c) {
+          float zs[32];
+          tmem_ld32(lane_base + static_cast<uint32_t>(sh * BN + c * 32), zs);
+          tmem_ld_wait();
+          const int vcols = g.Vb - (col_local + c * 32);  // columns of this chunk inside the vocabulary
+          uint32_t pk[16], pl[16];  // G in bf16 and (split) its bf16 rounding remainder
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float2 gv = __fmul2_rn(prob_diff2(make_float2(zt[2 * j], zt[2 * j + 1]),
-                                                make_float2(zs[2 * j], zs[2 * j + 1]), c2v, nbt, nbs, ngl2),
-                                     gs2);
-              if (vcols < 32) {  // the vocabulary ends inside this chunk: G = 0 past it
-                if (2 * j >= vcols) gv.x = 0.f;
-                if (2 * j + 1 >= vcols) gv.y = 0.f;
-              }
-              const uint32_t hi = pack_bf16x2(gv.x, gv.y);
-              pk[hh][j] = hi;
-              pl[hh][j] = pack_bf16x2(gv.x - __uint_as_float(hi << 16), gv.y - __uint_as_float(hi & 0xffff0000u));
+          for (int j = 0; j < 16; ++j) {
+            float2 gv = __fmul2_rn(prob_diff2(make_float2(zt[32 * c + 2 * j], zt[32 * c + 2 * j + 1]),
+                                              make_float2(zs[2 * j], zs[2 * j + 1]), c2v, nbt, nbs, ngl2),
+                                   gs2);
+            if (vcols < 32) {  // the vocabulary ends inside this chunk: G = 0 past it
+              if (2 * j >= vcols) gv.x = 0.f;
+              if (2 * j + 1 >= vcols) gv.y = 0.f;
             }
+            const uint32_t hi = pack_bf16x2(gv.x, gv.y);
+            pk[j] = hi;
+            if (SPLIT)
+              pl[j] = pack_bf16x2(gv.x - __uint_as_float(hi << 16), gv.y - __uint_as_float(hi & 0xffff0000u));
           }
-          for (int term = 0; term < (p.split ? 2 : 1); ++term) {
-            if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the staging rows
-            __syncwarp();
+          // 32 x 32 tiles of 64-byte rows, 64-byte swizzle (16-byte chunk i of row r at i ^ ((r >> 1) & 3));
+          // plain G alternates the two 2 KB tiles, split G puts bf16(G) in the first, the remainder in the second
+          const uint32_t buf = SPLIT ? 0u : static_cast<uint32_t>((c & 1) * 2048);
+          if (lane == 0) {
+            if (SPLIT)
+              bulk_wait_group_read<0>();
+            else
+              bulk_wait_group_read<1>();
+          }
+          __syncwarp();
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              const uint32_t chunk = static_cast<uint32_t>(c4 ^ (lane & 7));
-              const uint32_t* src = term == 0 ? &pk[c4 >> 2][4 * (c4 & 3)] : &pl[c4 >> 2][4 * (c4 & 3)];
-              st_shared_v4(rowaddr + chunk * 16, src[0], src[1], src[2], src[3]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && row_local < p.R) {
-              tma_store_3d(&maps.m[kMapG], staging, col_local + c2 * 64, row_local, g.slot + term * kGRing);
-              bulk_commit_group();
-            }
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t a = row64 + buf + ((static_cast<uint32_t>(i) ^ swz64) << 4);
+            st_shared_v4(a, pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            if (SPLIT) st_shared_v4(a + 2048, pl[4 * i], pl[4 * i + 1], pl[4 * i + 2], pl[4 * i + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row_local < p.R) {
+            tma_store_3d(&maps.m[kMapG], staging + buf, col_local + c * 32, row_local, g.slot);
+            if (SPLIT) tma_store_3d(&maps.m[kMapG], staging + 2048, col_local + c * 32, row_local, g.slot + kGRing);
+            bulk_commit_group();
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_remote(lead_tempty);
-          mbar_arrive_remote(lead_tempty + 8);
-        }
-        ++uses[0];
-        ++uses[1];
+        if (lane == 0) mbar_arrive_remote(lead_tempty + sh * 8);
       } else {
         ctr = 1u;
         const int h = hp;
@@ -699,12 +730,14 @@ cudaLaunchConfig_t pipe_config(cudaLaunchAttribute* attr, int clusters, cudaStre
 }  // namespace
 
 cudaError_t bwd_pipe_prepare(int* max_clusters) {
-  cudaError_t e = cudaFuncSetAttribute(bwd_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  cudaError_t e = cudaFuncSetAttribute(bwd_pipe_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bwd_pipe_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pipe_config(attr, 1, nullptr);
   cfg.numAttrs = 1;  // occupancy: the cluster shape only
-  return cudaOccupancyMaxActiveClusters(max_clusters, bwd_pipe_kernel, &cfg);
+  return cudaOccupancyMaxActiveClusters(max_clusters, bwd_pipe_kernel<false>, &cfg);
 }
 
 cudaError_t launch_bwd_pipe(const CUtensorMap* maps, const BwdPipeParams& p, int clusters, cudaStream_t stream) {
@@ -712,7 +745,8 @@ cudaError_t launch_bwd_pipe(const CUtensorMap* maps, const BwdPipeParams& p, int
   for (int m = 0; m < kPipeMaps; ++m) pm.m[m] = maps[m];
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pipe_config(attr, clusters, stream);
-  return cudaLaunchKernelEx(&cfg, bwd_pipe_kernel, pm, p);
+  return p.split ? cudaLaunchKernelEx(&cfg, bwd_pipe_kernel<true>, pm, p)
+                 : cudaLaunchKernelEx(&cfg, bwd_pipe_kernel<false>, pm, p);
 }
 
 }  // namespace hylo
