@@ -122,6 +122,31 @@ def kl_rows(h_s, W_s, h_t, W_t, tau: float, rows: Sequence[int], grad_scale: flo
 
 
 
+def kl_grad_vocab_rows(h_s, W_s, h_t, W_t, tau: float, vocab_rows: Sequence[int], lse_s, lse_t,
+                       grad_scale: float = 1.0, n_total: Optional[int] = None, token_chunk: int = 4096):
+    """Rows dW_s[v, :] of the student LM-head gradient for selected vocabulary rows v only,
+    given every token's log-sum-exps over the full vocabulary (as kl_forward returns them):
+    dW_s[v] = sum_n G[n, v] h_s[n] with G[n, v] = grad_scale (exp(z_s[n,v]/tau - lse_s[n]) -
+    exp(z_t[n,v]/tau - lse_t[n])) / (tau N), the column v of the G of kl_backward (the softmax
+    of each token needs the whole vocabulary only through its log-sum-exp).
+    Returns dW rows [len(vocab_rows), d_s]."""
+    rows = np.asarray(vocab_rows, dtype=np.int64)
+    N = h_s.shape[0]
+    n_total = N if n_total is None else n_total
+    Ws = np.asarray(W_s[rows], dtype=np.float64)
+    Wt = np.asarray(W_t[rows], dtype=np.float64)
+    lse_s = np.asarray(lse_s, dtype=np.float64)
+    lse_t = np.asarray(lse_t, dtype=np.float64)
+    out = np.zeros((len(rows), W_s.shape[1]))
+    for sl in _chunks(N, token_chunk):
+        hs = np.asarray(h_s[sl], dtype=np.float64)
+        zs = lm_head_logits(hs, Ws) / tau
+        zt = lm_head_logits(np.asarray(h_t[sl], dtype=np.float64), Wt) / tau
+        G = (np.exp(zs - lse_s[sl, None]) - np.exp(zt - lse_t[sl, None])) * (grad_scale / (tau * n_total))
+        out += G.T @ hs
+    return out
+
+
 def kl_from_logits(z_s, z_t, tau: float, grad_scale: float = 1.0):
     """The same loss on given logits ("Fused KL" of the digest's Key Ideas, applied to logits
     that were already projected): per-token KL(p_t || p_s), both log-sum-exps, the mean loss,

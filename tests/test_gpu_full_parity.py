@@ -1,0 +1,133 @@
+"""Full-size parity against the fp64 oracle's forward over EVERY token of a workload.
+
+For the 8K-token Llama-1B / 8B workload and the 16K-token Qwen-shaped workload (tau = 2) the
+oracle runs its plain forward over all N tokens (full vocabulary, materialised logits): the
+exact mean loss, every token's KL and both log-sum-exps. The GPU's outputs are compared with
+it everywhere. The gradients are compared on seeded rows the oracle computes one by one:
+512 token rows of dh_s (the oracle recomputes each row over the whole vocabulary) and 512
+vocabulary rows of dW_s (each a sum over all N tokens, from the ORACLE's log-sum-exps, so the
+check is independent of the GPU's statistics). The rows include the first and last ones, the
+edges of the 256-row tiles, of the backward's 4096- and 1024-token blocks and of its
+2560-word vocabulary blocks, and the last (ragged) vocabulary tile. The backward runs with
+token_chunk 4096 and 1000, so dW_s accumulates over 2 and 8 token blocks.
+
+Tolerances (stated for the fused hidden-state KL): per token |dKL| <= 1e-3 (1 + KL), mean loss
+1e-4 relative, gradients 2e-3 relative Frobenius (on the sampled rows); log-sum-exps
+2e-5 (1 + |lse|) (derived: fp32 logits of K <= 4096 bf16 products).
+"""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+from hybrid_upcycling_gb300 import _lib, build, synthetic as syn
+from oracle import kl_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+TOL_KL, TOL_LOSS, TOL_GRAD, TOL_LSE = 1e-3, 1e-4, 2e-3, 2e-5
+
+
+def f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+@pytest.fixture(scope="module", params=["llama1b_8b_8k", "qwen17b_8b"])
+def full_case(request):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    _lib.load()
+    w = syn.WORKLOADS[request.param]
+    x = syn.make_inputs(w, device="cuda")
+    a = {k: f64(v) for k, v in x.items()}
+    t0 = time.time()
+    kl, lse_s, lse_t, loss = orc.kl_forward(a["h_s"], a["W_s"], a["h_t"], a["W_t"], w.tau, token_chunk=1024)
+    print(f"\n{w.name}: oracle forward over all {w.N} tokens in {time.time() - t0:.0f} s, L = {loss:.9f}")
+    yield w, x, a, dict(kl=kl, lse_s=lse_s, lse_t=lse_t, loss=loss)
+    del x
+    torch.cuda.empty_cache()
+
+
+def gpu_forward(w, x):
+    dev = x["h_s"].device
+    N = w.N
+    ws = torch.empty(_lib.hylo_kl_workspace_bytes(N, w.d_s, w.d_t, w.V, 4096), dtype=torch.uint8, device=dev)
+    out = {k: torch.full((N,), float("nan"), device=dev) for k in ("kl", "lse_s", "lse_t", "gap")}
+    out["loss"] = torch.full((1,), float("nan"), device=dev)
+    _lib.hylo_kl_forward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, 4096, out["kl"], out["lse_s"], out["lse_t"],
+                         out["loss"], ws, lse_gap=out["gap"])
+    _lib.hylo_kl_sync_status()
+    return out
+
+
+def token_rows(N, k, seed):
+    fixed = {0, N - 1}
+    for edge in (128, 256, 1024, 4096):
+        for c in range(edge, N, edge * (4 if edge < 1024 else 1)):
+            fixed |= {c - 1, c}
+    fixed = sorted(fixed)[:k // 2]
+    rng = np.random.default_rng(seed)
+    rest = rng.choice(np.setdiff1d(np.arange(N), fixed), size=k - len(fixed), replace=False)
+    return np.array(sorted(set(fixed) | set(int(r) for r in rest)))
+
+
+def vocab_rows(V, k, seed):
+    last_tile = (V - 1) // 256 * 256
+    fixed = {0, 1, V - 1, V - 2, last_tile, last_tile - 1, 255, 256, 2559, 2560, 2561, 5119, 5120}
+    fixed |= {last_tile + 17, (V // 2560) * 2560, (V // 2560) * 2560 - 1}
+    fixed = {v for v in fixed if 0 <= v < V}
+    rng = np.random.default_rng(seed)
+    rest = rng.choice(np.setdiff1d(np.arange(V), sorted(fixed)), size=k - len(fixed), replace=False)
+    return np.array(sorted(fixed | set(int(r) for r in rest)))
+
+
+def test_full_forward_against_every_token(full_case):
+    w, x, _, ref = full_case
+    g = gpu_forward(w, x)
+    kl, ls, lt = f64(g["kl"]), f64(g["lse_s"]), f64(g["lse_t"])
+    e_kl = np.max(np.abs(kl - ref["kl"]) / (1 + ref["kl"]))
+    e_loss = abs(g["loss"].item() - ref["loss"]) / ref["loss"]
+    e_ls = np.max(np.abs(ls - ref["lse_s"]) / (1 + np.abs(ref["lse_s"])))
+    e_lt = np.max(np.abs(lt - ref["lse_t"]) / (1 + np.abs(ref["lse_t"])))
+    e_gap = np.max(np.abs(f64(g["gap"]) - (ref["lse_s"] - ref["lse_t"])) / (1 + np.abs(ref["lse_s"])))
+    print(f"{w.name}: all {w.N} tokens: kl {e_kl:.2e} (tol {TOL_KL}), mean loss {e_loss:.2e} (tol {TOL_LOSS}), "
+          f"lse_s {e_ls:.2e}, lse_t {e_lt:.2e}, gap {e_gap:.2e} (tol {TOL_LSE})")
+    assert e_kl <= TOL_KL
+    assert e_loss <= TOL_LOSS
+    assert e_ls <= TOL_LSE and e_lt <= TOL_LSE and e_gap <= TOL_LSE
+
+
+def test_full_backward_sampled_rows(full_case):
+    w, x, a, ref = full_case
+    g = gpu_forward(w, x)
+    rows_n = token_rows(w.N, 512, w.seed + 11)
+    rows_v = vocab_rows(w.V, 512, w.seed + 13)
+    gs = 0.75
+    t0 = time.time()
+    _, _, _, dh_ref = orc.kl_rows(a["h_s"], a["W_s"], a["h_t"], a["W_t"], w.tau, rows_n, grad_scale=gs)
+    dW_ref = orc.kl_grad_vocab_rows(a["h_s"], a["W_s"], a["h_t"], a["W_t"], w.tau, rows_v, ref["lse_s"],
+                                    ref["lse_t"], grad_scale=gs)
+    print(f"\n{w.name}: oracle rows in {time.time() - t0:.0f} s")
+    dev = x["h_s"].device
+    for chunk in (4096, 1000):
+        ws = torch.empty(_lib.hylo_kl_workspace_bytes(w.N, w.d_s, w.d_t, w.V, chunk), dtype=torch.uint8, device=dev)
+        dh = torch.full((w.N, w.d_s), float("nan"), device=dev)
+        dW = torch.full((w.V, w.d_s), float("nan"), device=dev)
+        _lib.hylo_kl_backward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, chunk, g["lse_s"], g["lse_t"], gs, dh, dW,
+                              ws, lse_gap=g["gap"])
+        _lib.hylo_kl_sync_status()
+        assert torch.all(torch.isfinite(dh)) and torch.all(torch.isfinite(dW))
+        rn = torch.from_numpy(rows_n).to(dev)
+        rv = torch.from_numpy(rows_v).to(dev)
+        e_dh = float(np.linalg.norm(f64(dh[rn]) - dh_ref) / np.linalg.norm(dh_ref))
+        e_dW = float(np.linalg.norm(f64(dW[rv]) - dW_ref) / np.linalg.norm(dW_ref))
+        # the worst single row, for the record
+        r_dW = np.max(np.linalg.norm(f64(dW[rv]) - dW_ref, axis=1) / np.linalg.norm(dW_ref, axis=1))
+        print(f"{w.name} chunk {chunk}: dh_s {len(rows_n)} rows {e_dh:.2e}, dW_s {len(rows_v)} vocabulary rows "
+              f"{e_dW:.2e} (worst row {r_dW:.2e}); tol {TOL_GRAD}")
+        assert e_dh <= TOL_GRAD
+        assert e_dW <= TOL_GRAD
+        del dh, dW, ws
+        torch.cuda.empty_cache()

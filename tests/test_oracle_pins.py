@@ -239,6 +239,25 @@ def test_rows_match_full():
     np.testing.assert_allclose(dhr, dh[rows], rtol=1e-12, atol=1e-16)
 
 
+def test_vocab_rows_match_full():
+    """dW_s rows from the per-token log-sum-exps alone equal the rows of the full backward (a
+    slip in the column's softmax, the 1/(tau N) or the transpose fails this), over several token
+    chunks and with a global N larger than the rows passed."""
+    rng = np.random.default_rng(43)
+    h_s, W_s, h_t, W_t = _rand_problem(rng, 23, 6, 8, 31)
+    _, lse_s, lse_t, _ = orc.kl_forward(h_s, W_s, h_t, W_t, 0.7)
+    _, dW = orc.kl_backward(h_s, W_s, h_t, W_t, 0.7, grad_scale=-1.5)
+    rows = [0, 30, 5, 17, 5]
+    got = orc.kl_grad_vocab_rows(h_s, W_s, h_t, W_t, 0.7, rows, lse_s, lse_t, grad_scale=-1.5, token_chunk=4)
+    np.testing.assert_allclose(got, dW[rows], rtol=1e-11, atol=1e-16)
+    # a token subset of a larger mean: its share of the full gradient, scaled by N_sub / N
+    sub = orc.kl_grad_vocab_rows(h_s[:9], W_s, h_t[:9], W_t, 0.7, rows, lse_s[:9], lse_t[:9], grad_scale=-1.5,
+                                 n_total=23)
+    rest = orc.kl_grad_vocab_rows(h_s[9:], W_s, h_t[9:], W_t, 0.7, rows, lse_s[9:], lse_t[9:], grad_scale=-1.5,
+                                  n_total=23)
+    np.testing.assert_allclose(sub + rest, dW[rows], rtol=1e-11, atol=1e-16)
+
+
 # ----------------------------------------------------------------------------- statistics
 
 def _f64(t):
