@@ -28,10 +28,12 @@
 // running CTA, so the launch cannot deadlock whatever the residency; in this order the waits
 // almost never block.
 //
-// Roles (384 threads per CTA of a cluster pair): warp 0 of the even CTA takes items from the
-// queue and publishes them to both CTAs through a small shared-memory item ring; warp 0 of each
-// CTA waits for the item's dependencies and issues its TMA loads; warp 1 of the even CTA issues
-// the UMMAs; warps 4..11 of both CTAs are the epilogue (lane quarter w & 3, column half
+// Roles (384 threads per CTA of a cluster pair): warp 2 of the even CTA takes items from the
+// queue, waits for their dependencies and publishes them to both CTAs through a shared-memory
+// item ring, up to kItemDepth items ahead of the loads, so that the global-memory round trips of
+// the queue and the counters stay off the path between two items' TMA loads; warp 0 of each CTA
+// issues the TMA loads; warp 1 of the even CTA issues the UMMAs; warps 4..11 of both CTAs are
+// the epilogue (lane quarter w & 3, column half
 // (w - 4) >> 2 of each 256-column accumulator). Warpgroup 0 gives registers to the two epilogue
 // warpgroups (setmaxnreg: 56 and 224 per thread).
 //
@@ -65,7 +67,7 @@ constexpr int STAGES = 6;
 // per epilogue warp: 32 rows x 128 B (M items: 32 fp32 columns, 128-byte swizzle; F items: two
 // tiles of 32 rows x 32 bf16 columns, 64-byte swizzle)
 constexpr int STAGING_BYTES = kEpiWarps * 4096;
-constexpr int kItemDepth = 4;
+constexpr int kItemDepth = 3;
 constexpr int ITEM_OFF = STAGES * STAGE_BYTES + STAGING_BYTES;
 constexpr int BAR_OFF = ITEM_OFF + kItemDepth * 32;
 // full[S], empty[S], tfull[2], tempty[2], ifull[D], iempty[D], drain
@@ -74,9 +76,9 @@ constexpr int NBARS = 2 * STAGES + 4 + 2 * kItemDepth + 1;
 constexpr int SMEM = 1024 + BAR_OFF + NBARS * 8 + 8 + 4 * kEpiWarps;
 static_assert(SMEM <= 232448, "shared memory budget");
 
-// Threads that release an item-ring slot: the even CTA's UMMA thread and epilogue warps, the
-// odd CTA's producer and epilogue warps.
-constexpr int kItemConsumers = 2 * (1 + kEpiWarps);
+// Threads that release an item-ring slot: in each CTA the producer and the epilogue warps, and
+// the even CTA's UMMA thread.
+constexpr int kItemConsumers = 2 * (1 + kEpiWarps) + 1;
 
 enum : int { kItemF = 0, kItemDW = 1, kItemDH = 2, kItemEnd = 3 };
 // kMapG: G tile stores, box 32 x 32 words with 64-byte swizzle
@@ -310,92 +312,137 @@ bwd_pipe_kernel(const __grid_constant__ PipeMaps maps, const BwdPipeParams p) {
   const int kbt = p.kb_t, kbf = p.kb_t + p.kb_s;
 
   if (warp < kEpiWarp0) setmaxnreg_dec<kRegsControl>();  // each warpgroup changes its registers at once
-  if (warp == 0) {
-    // ------------------------------------------- scheduler (even CTA) and TMA producer (both CTAs)
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0, armed = 0;
-      bool ok = true;
+  if (warp == 2) {
+    // ------------------------------------------------------------------ scheduler (even CTA)
+    if (lane == 0 && rank == 0) {
       Cursor cur;
       cursor_init(cur, p);
       const uint32_t peer_items = mapa_shared(smem_u32(items), 1);
       const uint32_t peer_ifull = mapa_shared(smem_u32(ifull), 1);
+      int next_i = static_cast<int>(atomicAdd(p.ctrl, 1u));
+      for (int k = 0;; ++k) {
+        const int slot = k % kItemDepth;
+        const uint32_t par = static_cast<uint32_t>(k / kItemDepth) & 1u;
+        if (!wait_bounded<true>(iempty + slot, par ^ 1u, abort_flag, p.ctl, 21)) break;
+        const Item it = cursor_item(cur, p, next_i);
+        if (it.kind != kItemEnd) {
+          next_i = static_cast<int>(atomicAdd(p.ctrl, 1u));  // the next item, fetched ahead
+          // the item is published only once what it reads is complete
+          if (!wait_count(p.ctrl, it.ctr0, it.tgt0, abort_flag, p.ctl, 23) ||
+              !wait_count(p.ctrl, it.ctr1, it.tgt1, abort_flag, p.ctl, 24))
+            break;
+        }
+        items[slot] = it;
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&it);
+        for (int q = 0; q < 8; ++q) st_cluster_u32(peer_items + slot * 32 + q * 4, w[q]);
+        mbar_arrive(ifull + slot);
+        mbar_arrive_remote(peer_ifull + slot * 8);
+        if (it.kind == kItemEnd) break;
+      }
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, armed = 0;
+      bool ok = true;
       const uint32_t lead_iempty = mapa_shared(smem_u32(iempty), 0);
-      int next_i = rank == 0 ? static_cast<int>(atomicAdd(p.ctrl, 1u)) : 0;
+      const uint32_t full_lead = mapa_shared(smem_u32(full), 0);  // full[0] of the even CTA
       for (int k = 0; ok; ++k) {
         const int slot = k % kItemDepth;
         const uint32_t par = static_cast<uint32_t>(k / kItemDepth) & 1u;
-        Item it;
-        if (rank == 0) {
-          if (!wait_bounded<true>(iempty + slot, par ^ 1u, abort_flag, p.ctl, 21)) break;
-          it = cursor_item(cur, p, next_i);
-          items[slot] = it;
-          const uint32_t* w = reinterpret_cast<const uint32_t*>(&it);
-          for (int q = 0; q < 8; ++q) st_cluster_u32(peer_items + slot * 32 + q * 4, w[q]);
-          mbar_arrive(ifull + slot);
-          mbar_arrive_remote(peer_ifull + slot * 8);
-          if (it.kind == kItemEnd) break;
-          next_i = static_cast<int>(atomicAdd(p.ctrl, 1u));  // the next item, fetched ahead
-        } else {
-          if (!wait_bounded<true>(ifull + slot, par, abort_flag, p.ctl, 22)) break;
-          it = items[slot];
+        if (!wait_bounded<true>(ifull + slot, par, abort_flag, p.ctl, 22)) break;
+        const Item it = items[slot];
+        if (rank == 0)
+          mbar_arrive(iempty + slot);
+        else
           mbar_arrive_remote(lead_iempty + slot * 8);
-          if (it.kind == kItemEnd) break;
-        }
-        if (!wait_count(p.ctrl, it.ctr0, it.tgt0, abort_flag, p.ctl, 23) ||
-            !wait_count(p.ctrl, it.ctr1, it.tgt1, abort_flag, p.ctl, 24)) {
-          ok = false;
-          break;
-        }
-        fence_proxy_async_global();  // the G tiles other CTAs stored are read by TMA below
+        if (it.kind == kItemEnd) break;
+        // the G tiles this item reads were stored by TMA in other CTAs, whose completion the
+        // scheduler observed (acquire) before publishing the item
+        fence_proxy_async_global();
+        // Every coordinate is set up once per item: a stage then costs only its wait, its arming
+        // and its TMA instructions (the producer, not the tensor cores, limited the M items while
+        // it also did this arithmetic per stage).
         const Geo g = geo(p, it.b);
-        const int nkb = it.kind == kItemF ? kbf : m_kblocks<SPLIT>(g, it.kind);
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bounded(empty + stage, phase ^ 1u, abort_flag, p.ctl, 25)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sa = smem + stage * STAGE_BYTES;
-          uint8_t* sb = sa + A_BYTES;
-          const uint32_t fbar = mapa_shared(smem_u32(full + stage), 0);
+        const int r_a = static_cast<int>(rank) * kBM;  // this CTA's rows of the A tile
+        const int r_b = static_cast<int>(rank) * HB;   // this CTA's rows of the B tile
+        bool fine = true;
+        auto next = [&](uint8_t*& sa, uint32_t& fb) -> bool {  // wait for a free stage and arm it
+          if (!wait_bounded(empty + stage, phase ^ 1u, abort_flag, p.ctl, 25)) return false;
+          sa = smem + stage * STAGE_BYTES;
+          fb = full_lead + static_cast<uint32_t>(stage) * 8u;
           if (rank == 0) {
             mbar_arrive_expect_tx(full + stage, 2 * STAGE_BYTES);  // both CTAs' bytes
             armed |= 1u << stage;
           }
-          if (it.kind == kItemF) {
-            const int ti = it.idx % g.tt, vi = it.idx / g.tt;
-            const int arow = g.r0 + ti * BN + static_cast<int>(rank) * kBM;
-            const int brow = g.v0 + vi * BN + static_cast<int>(rank) * HB;
-            if (kb < kbt) {
-              tma_load_2d_pair(sa, &maps.m[kMapHt], fbar, kb * kBK, arow);
-              tma_load_2d_pair(sb, &maps.m[kMapWt], fbar, kb * kBK, brow);
-            } else {
-              tma_load_2d_pair(sa, &maps.m[kMapHs], fbar, (kb - kbt) * kBK, arow);
-              tma_load_2d_pair(sb, &maps.m[kMapWs], fbar, (kb - kbt) * kBK, brow);
-            }
-          } else {
-            const int half = SPLIT ? nkb / 2 : nkb;
-            const int kk = kb < half ? kb : kb - half;
-            const int z = g.slot + (kb < half ? 0 : kGRing);
-            const int mi = it.idx / p.ntd, nj = it.idx - (it.idx / p.ntd) * p.ntd;
-            const int ncol = nj * BN + static_cast<int>(rank) * HB;  // this CTA's d_s columns (B rows)
-            if (it.kind == kItemDW) {  // A = G^T (vocabulary-major), B = h_s of the block's tokens
-              const int mrow = mi * BN + static_cast<int>(rank) * kBM;
-              tma_load_3d_pair(sa, &maps.m[kMapGT], fbar, mrow, kk * kBK, z);
-              tma_load_3d_pair(sa + 8192, &maps.m[kMapGT], fbar, mrow + 64, kk * kBK, z);
-              tma_load_2d_pair(sb, &maps.m[kMapHsB], fbar, ncol, g.r0 + kk * kBK);
-              tma_load_2d_pair(sb + 8192, &maps.m[kMapHsB], fbar, ncol + 64, g.r0 + kk * kBK);
-            } else {  // A = G (token rows, K-major), B = W_s of the block's words
-              const int mrow = mi * BN + static_cast<int>(rank) * kBM;
-              tma_load_3d_pair(sa, &maps.m[kMapGA], fbar, kk * kBK, mrow, z);
-              tma_load_2d_pair(sb, &maps.m[kMapWsB], fbar, ncol, g.v0 + kk * kBK);
-              tma_load_2d_pair(sb + 8192, &maps.m[kMapWsB], fbar, ncol + 64, g.v0 + kk * kBK);
-            }
-          }
+          return true;
+        };
+        auto advance = [&]() {
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
+        };
+        if (it.kind == kItemF) {  // teacher tile over d_t, then student tile over d_s
+          const int ti = it.idx % g.tt, vi = it.idx / g.tt;
+          const int arow = g.r0 + ti * BN + r_a, brow = g.v0 + vi * BN + r_b;
+          for (int kb = 0; fine && kb < kbt; ++kb) {
+            uint8_t* sa;
+            uint32_t fb;
+            if (!(fine = next(sa, fb))) break;
+            tma_load_2d_pair(sa, &maps.m[kMapHt], fb, kb * kBK, arow);
+            tma_load_2d_pair(sa + A_BYTES, &maps.m[kMapWt], fb, kb * kBK, brow);
+            advance();
+          }
+          for (int kb = 0; fine && kb < p.kb_s; ++kb) {
+            uint8_t* sa;
+            uint32_t fb;
+            if (!(fine = next(sa, fb))) break;
+            tma_load_2d_pair(sa, &maps.m[kMapHs], fb, kb * kBK, arow);
+            tma_load_2d_pair(sa + A_BYTES, &maps.m[kMapWs], fb, kb * kBK, brow);
+            advance();
+          }
+        } else {
+          const int mi = it.idx / p.ntd, nj = it.idx - mi * p.ntd;
+          const int mrow = mi * BN + r_a;   // A rows: words (dW_s) or tokens (dh_s) of the block
+          const int ncol = nj * BN + r_b;   // B rows: this CTA's d_s columns
+          if (it.kind == kItemDW) {  // A = G^T (word-major), B = h_s of the block's tokens; K = tokens
+            const int nk = (g.R + kBK - 1) / kBK;
+            for (int term = 0; fine && term < (SPLIT ? 2 : 1); ++term) {
+              const int z = g.slot + term * kGRing;
+              for (int kk = 0; kk < nk; ++kk) {
+                uint8_t* sa;
+                uint32_t fb;
+                if (!(fine = next(sa, fb))) break;
+                const int k0 = kk * kBK;
+                tma_load_3d_pair(sa, &maps.m[kMapGT], fb, mrow, k0, z);
+                tma_load_3d_pair(sa + 8192, &maps.m[kMapGT], fb, mrow + 64, k0, z);
+                tma_load_2d_pair(sa + A_BYTES, &maps.m[kMapHsB], fb, ncol, g.r0 + k0);
+                tma_load_2d_pair(sa + A_BYTES + 8192, &maps.m[kMapHsB], fb, ncol + 64, g.r0 + k0);
+                advance();
+              }
+            }
+          } else {  // A = G (token rows, K-major), B = W_s of the block's words; K = words
+            const int nk = (g.Vb + kBK - 1) / kBK;
+            for (int term = 0; fine && term < (SPLIT ? 2 : 1); ++term) {
+              const int z = g.slot + term * kGRing;
+              for (int kk = 0; kk < nk; ++kk) {
+                uint8_t* sa;
+                uint32_t fb;
+                if (!(fine = next(sa, fb))) break;
+                const int k0 = kk * kBK;
+                tma_load_3d_pair(sa, &maps.m[kMapGA], fb, k0, mrow, z);
+                tma_load_2d_pair(sa + A_BYTES, &maps.m[kMapWsB], fb, ncol, g.v0 + k0);
+                tma_load_2d_pair(sa + A_BYTES + 8192, &maps.m[kMapWsB], fb, ncol + 64, g.v0 + k0);
+                advance();
+              }
+            }
+          }
+        }
+        if (!fine) {
+          ok = false;
+          break;
         }
       }
       if (!ok) {

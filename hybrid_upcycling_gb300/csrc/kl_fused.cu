@@ -12,12 +12,16 @@
 // next-token distributions, kl_weight 1.0, no cross-entropy (HyLo-Llama-8MLA8GDN-8K-SFT reading
 // notes, kwkr.cn, section "two-stage training recipe", Stage II).
 //
-// Roles (320 threads per CTA): warp 0 issues the TMA loads, warp 1 of the even CTA owns TMEM
-// and issues the UMMAs for the pair, warps 2..9 are the epilogue. Warp w may read only TMEM
-// lanes 32*(w%4) .. 32*(w%4)+31, so each epilogue thread owns one token row of its CTA's
-// 128-row tile: warps 2..5 take columns 0..127 of the 256-column tile, warps 6..9 columns
-// 128..255 (lane quarter w & 3, column half (w - 2) >> 2). The (teacher, student) accumulator
-// pair fills TMEM and is drained between tiles.
+// Roles (384 threads per CTA): warp 0 issues the TMA loads, warp 1 of the even CTA owns TMEM
+// and issues the UMMAs for the pair, warps 4..11 are the epilogue (warpgroup 0 gives registers
+// to the two epilogue warpgroups: setmaxnreg 56 / 224). Warp w may read only TMEM lanes
+// 32*(w%4) .. 32*(w%4)+31, so each epilogue thread owns one token row of its CTA's 128-row
+// tile: warps 4..7 take columns 0..127 of the 256-column tile, warps 8..11 columns 128..255.
+// TMEM: the teacher tile in columns 0..255 (half 0), the student tile in 256..511 (half 1).
+// The UMMA warp signals half 0 as soon as the teacher UMMAs are done; the epilogue copies its
+// row's 128 teacher logits into registers and frees half 0, so the next tile's teacher UMMAs
+// (two thirds of its work at d_t = 2 d_s) run while the epilogue folds the student tile, and
+// half 1 is free again long before the next student UMMAs.
 #include <cfloat>
 #include <cmath>
 
@@ -28,20 +32,23 @@ namespace hylo {
 namespace {
 
 constexpr int kEpiWarps = 8;                   // two per TMEM lane quarter, one per column half
-constexpr int kThreads = 64 + 32 * kEpiWarps;  // + TMA warp + UMMA warp
+constexpr int kEpiWarp0 = 4;                   // first epilogue warp (warpgroups 1 and 2)
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kRegsControl = 56;               // per thread, warpgroup 0 (TMA, UMMA)
+constexpr int kRegsEpilogue = 224;             // per thread, warpgroups 1 and 2
+static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= kThreads * 168, "register split");
 
 // A CTA pair (cluster of 2 on an SM pair) computes a 256-token x BN-word tile with one
 // tcgen05.mma.cta_group::2 per 16-deep slice (M = 256): each CTA stages its 128 token rows of
 // h and BN/2 rows of W, and each CTA's TMEM holds its 128 rows of the teacher and student
-// tiles. kFusedBN = 256: one (teacher, student) pair fills the 512 TMEM columns and is drained
-// between tiles. (BN = 128 would fit two pairs and overlap the epilogue with the next tile's
-// UMMAs, but N = 128 UMMAs measured 22% slower end to end on GB300, on one CTA or on a pair.)
+// tiles. kFusedBN = 256: one (teacher, student) pair fills the 512 TMEM columns. (BN = 128
+// would fit two pairs, but N = 128 UMMAs measured 22% slower end to end on GB300, on one CTA
+// or on a pair.)
 template <int BN_>
 struct FusedCfg {
   static constexpr int BN = BN_;         // vocabulary columns per pair tile
   static constexpr int HB = BN / 2;      // W rows staged per CTA
   static constexpr int HALF = BN / 2;    // columns per epilogue warp
-  static constexpr int NBUF = 512 / (2 * BN);
   static constexpr int A_BYTES = kBM * kBK * 2;
   static constexpr int B_BYTES = HB * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -49,10 +56,10 @@ struct FusedCfg {
   // the statistics of one column half handed to the other half at a unit's end
   static constexpr int EXTRA_BYTES = kStatFields * kBM * 4;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES + EXTRA_BYTES;
-  // full[S], empty[S], tfull[NBUF], tempty[NBUF], merge_full, merge_empty, drain
-  static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 3;
+  // full[S], empty[S], tfull[2], tempty[2] (teacher half, student half), merge_full, merge_empty, drain
+  static constexpr int NBARS = 2 * STAGES + 4 + 3;
   static constexpr int SMEM = 1024 + BAR_OFF + NBARS * 8 + 16;
-  static_assert(NBUF >= 1 && HALF % 64 == 0 && HB % 8 == 0, "tile shape");
+  static_assert(2 * BN == 512 && HALF % 64 == 0 && HB % 8 == 0, "tile shape");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -110,15 +117,14 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
   constexpr int BN = C::BN;
   constexpr int HB = C::HB;
   constexpr int HALF = C::HALF;
-  constexpr int NBUF = C::NBUF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* extra = smem + C::STAGES * C::STAGE_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);  // used in the even CTA
   uint64_t* empty = full + C::STAGES;       // both CTAs: stage free (UMMAs done reading it)
-  uint64_t* tfull = empty + C::STAGES;      // both CTAs: tile pair in TMEM buffer b complete
-  uint64_t* tempty = tfull + NBUF;          // even CTA: buffer b drained by both epilogues
-  uint64_t* merge_full = tempty + NBUF;     // forward: column half 1 -> half 0 statistics handoff
+  uint64_t* tfull = empty + C::STAGES;      // both CTAs: TMEM half h (0 teacher, 1 student) complete
+  uint64_t* tempty = tfull + 2;             // even CTA: half h read by both CTAs' epilogues
+  uint64_t* merge_full = tempty + 2;        // column half 1 -> half 0 statistics handoff
   uint64_t* merge_empty = merge_full + 1;
   uint64_t* drain = merge_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -135,7 +141,7 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
-    for (int b = 0; b < NBUF; ++b) {
+    for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
       mbar_init(tempty + b, 2 * kEpiWarps);  // every epilogue warp of both CTAs
     }
@@ -167,6 +173,7 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
   const int kbt = p.kb_t, kbtot = p.kb_t + p.kb_s;
   const int my_rows = static_cast<int>(rank) * kBM;  // this CTA's token rows inside a pair tile
 
+  if (warp < kEpiWarp0) setmaxnreg_dec<kRegsControl>();  // each warpgroup changes its registers at once
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
@@ -261,8 +268,8 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ UMMA issuer (even CTA)
-    // Teacher tile (K = d_t) then student tile (K = d_s) into TMEM buffer b of both CTAs:
-    // teacher in columns [2*BN*b, 2*BN*b + BN), student in the next BN columns.
+    // Teacher tile (K = d_t) into half 0, then student tile (K = d_s) into half 1 of both CTAs;
+    // each half is awaited just before its own UMMAs and signalled as soon as they are done.
     if (lane == 0 && rank == 0) {
       constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, BN, false, false);
       int stage = 0;
@@ -273,16 +280,16 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
         int row0, vt0, vt1, seg;
         unit_range(p, u, row0, vt0, vt1, seg);
         for (int vt = vt0; ok && vt < vt1; ++vt, ++lt) {
-          const int b = lt % NBUF;
-          const uint32_t tph = static_cast<uint32_t>(lt / NBUF) & 1u;
-          if (!wait_bounded(tempty + b, tph ^ 1u, abort_flag, p.ctl, 2)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t dT = tmem_base + static_cast<uint32_t>(b * 2 * BN);
-          const uint32_t dS = dT + BN;
+          const uint32_t tph = static_cast<uint32_t>(lt) & 1u;
           for (int kb = 0; kb < kbtot; ++kb) {
+            if (kb == 0 || kb == kbt) {
+              if (kb == kbt) umma_commit_pair(tfull + 0, 0x3);
+              if (!wait_bounded(tempty + (kb == 0 ? 0 : 1), tph ^ 1u, abort_flag, p.ctl, 2)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
             if (!wait_bounded(full + stage, phase, abort_flag, p.ctl, 3)) {
               ok = false;
               break;
@@ -291,7 +298,7 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
             const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
             const uint32_t sb = sa + C::A_BYTES;
             const bool teacher = kb < kbt;
-            const uint32_t d = teacher ? dT : dS;
+            const uint32_t d = tmem_base + (teacher ? 0u : static_cast<uint32_t>(BN));
             const int kk = teacher ? kb : kb - kbt;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
@@ -306,7 +313,7 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
             }
           }
           if (!ok) break;
-          umma_commit_pair(tfull + b, 0x3);
+          umma_commit_pair(tfull + 1, 0x3);
         }
       }
       if (!ok && issued) {
@@ -314,9 +321,10 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
         drain_wait(drain, 0, 100000000ull);
       }
     }
-  } else {
+  } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
-    const int e = warp - 2;         // 0..7
+    setmaxnreg_inc<kRegsEpilogue>();
+    const int e = warp - kEpiWarp0;  // 0..7
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     const int h = e >> 2;           // column half of the tile: [h*HALF, h*HALF + HALF)
     const int row = q * 32 + lane;  // token row inside this CTA's 128 rows
@@ -330,33 +338,44 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
       const int token = row0 + my_rows + row;
       RowStats rs{-INFINITY, 0.f, -INFINITY, 0.f, 0.f, 0.f, false};
       for (int vt = vt0; vt < vt1; ++vt, ++lt) {
-        const int b = lt % NBUF;
-        const uint32_t tph = static_cast<uint32_t>(lt / NBUF) & 1u;
-        bool w = wait_bounded(tfull + b, tph, abort_flag, p.ctl, 4);
+        const uint32_t tph = static_cast<uint32_t>(lt) & 1u;
+        // the teacher tile: this row's 128 logits of the column half into registers, then half 0
+        // goes back to the UMMAs
+        bool w = wait_bounded(tfull + 0, tph, abort_flag, p.ctl, 4);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t tT = lane_base + static_cast<uint32_t>(b * 2 * BN);
-        const uint32_t tS = tT + BN;
+        float zt[HALF];
+#pragma unroll
+        for (int c = 0; c < HALF / 32; ++c) tmem_ld32_at(lane_base + static_cast<uint32_t>(c * 32), zt + 32 * c);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + 0), 0));
+        w = wait_bounded(tfull + 1, tph, abort_flag, p.ctl, 4);
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         const int col_base = vt * BN + h * HALF;
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < HALF / 32; ++c) {
-          float zt[32], zs[32];
-          tmem_ld32(tT + c * 32, zt);
-          tmem_ld32(tS + c * 32, zs);
+          float zs[32];
+          tmem_ld32(lane_base + static_cast<uint32_t>(BN + c * 32), zs);
           tmem_ld_wait();
           const int valid = min(32, p.V - (col_base + c * 32));
           if (valid >= 32) {
-            fold_chunk<false>(rs, zt, zs, 0xffffffffu, p.c, p.inv_tau);
+            fold_chunk<false>(rs, zt + 32 * c, zs, 0xffffffffu, p.c, p.inv_tau);
           } else if (valid > 0) {
-            fold_chunk<true>(rs, zt, zs, (1u << valid) - 1u, p.c, p.inv_tau);
+            fold_chunk<true>(rs, zt + 32 * c, zs, (1u << valid) - 1u, p.c, p.inv_tau);
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + b), 0));
+        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + 1), 0));
       }
       if (!ok) break;
       // column half 1 hands its statistics to half 0, which merges and writes them

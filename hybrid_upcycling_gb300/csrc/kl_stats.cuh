@@ -46,9 +46,10 @@ __device__ __forceinline__ float2 ex2_approx2(float2 x) { return make_float2(ex2
 // Each column adds e_t g(d) to C: the Taylor series for |d| < 1/4, otherwise
 // e_t (exp(-d) - 1 + d) = e_s K - e_t + e_t d with K = exp((m_s - m_t)/tau), which uses no
 // extra exponential. K is clamped to stay finite; if the clamp engages the row is marked far.
+// zt_in, zs_in: 32 consecutive values each (register arrays indexed with compile-time offsets).
 template <bool MASKED>
-__device__ __forceinline__ void fold_chunk(RowStats& r, const float (&zt_in)[32], const float (&zs_in)[32],
-                                           uint32_t valid, float c, float inv_tau) {
+__device__ __forceinline__ void fold_chunk(RowStats& r, const float* zt_in, const float* zs_in, uint32_t valid,
+                                           float c, float inv_tau) {
   float cmt = -INFINITY, cms = -INFINITY;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
