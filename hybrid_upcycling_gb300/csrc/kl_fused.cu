@@ -201,30 +201,48 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           const int brow = vt * BN + static_cast<int>(rank) * HB;
           if (pace) {
+            // One poll reads every peer that is still behind with independent loads (eight at a
+            // time), so a check costs about one round trip to L2 rather than one per peer.
             volatile unsigned long long* prog = p.progress;
             const unsigned long long mine = (kunit << 24) | static_cast<unsigned long long>(vt - vt0);
             prog[cid] = ep | mine;
             const uint64_t t0 = globaltimer_ns();
-            bool off = prog[kMaxClusters] == ep;
-            for (int w = 0; !off && w < kMaxClusters / 32; ++w) {
-              for (uint32_t bits = peers[w]; !off && bits != 0u; bits &= bits - 1u) {
-                const int j = 32 * w + __ffs(static_cast<int>(bits)) - 1;
-                while (true) {
-                  const unsigned long long v = prog[j];
-                  if ((v & ~kPaceLow) == ep) {  // the peer has started this launch
+            uint32_t pend[kMaxClusters / 32];
+#pragma unroll
+            for (int w = 0; w < kMaxClusters / 32; ++w) pend[w] = peers[w];
+            while (true) {
+              if (prog[kMaxClusters] == ep) break;  // pacing was given up for this launch
+              bool behind = false;
+#pragma unroll 1
+              for (int w = 0; w < kMaxClusters / 32; ++w) {
+                uint32_t bits = pend[w];
+                while (bits != 0u) {
+                  int js[8];
+                  unsigned long long vs[8];
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) {
+                    js[i] = bits != 0u ? 32 * w + __ffs(static_cast<int>(bits)) - 1 : -1;
+                    bits &= bits - 1u;
+                  }
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) vs[i] = js[i] >= 0 ? prog[js[i]] : 0ull;
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) {
+                    if (js[i] < 0) continue;
+                    const unsigned long long v = vs[i];
                     const unsigned long long lo = v & kPaceLow;
-                    if (lo == kPaceLow || lo + kPaceLead >= mine) break;
-                  }
-                  if (globaltimer_ns() - t0 > kPaceWaitNs) {  // give up pacing for the whole launch
-                    prog[kMaxClusters] = ep;
-                    off = true;
-                    break;
-                  }
-                  if (prog[kMaxClusters] == ep) {
-                    off = true;
-                    break;
+                    // a peer of this launch (its epoch tag) that finished or is at most kPaceLead tiles behind
+                    if ((v & ~kPaceLow) == ep && (lo == kPaceLow || lo + kPaceLead >= mine))
+                      pend[w] &= ~(1u << (js[i] & 31));
+                    else
+                      behind = true;
                   }
                 }
+              }
+              if (!behind) break;
+              if (globaltimer_ns() - t0 > kPaceWaitNs) {  // give up pacing for the whole launch
+                prog[kMaxClusters] = ep;
+                break;
               }
             }
           }
