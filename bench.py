@@ -6,9 +6,13 @@ token_chunk=4096). Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-Under torchrun each rank runs an independent replica of the workload on its own GPU (the
-loss needs no exchange on one GPU; weak scaling). `--impl reference` times the fp64 CPU
-oracle on the host cores on a bounded token sample of the same workload.
+Under torchrun (N > 1) the default `--mode dp` is the data-parallel step of Stage-II training:
+every rank holds its own sequence of the workload's N tokens (one global batch of N x ranks
+tokens) and the full LM heads, runs the forward + backward through the C ABI with
+grad_scale = N / (N x ranks), and the ranks exchange the loss sum and dW_s with one NCCL
+all-reduce each (hybrid_upcycling_gb300.shard; weak scaling, the collectives inside the timed
+region). `--mode replicas` runs independent replicas instead (no exchange). `--impl reference`
+times the fp64 CPU oracle on the host cores on a bounded token sample of the same workload.
 """
 from __future__ import annotations
 
@@ -541,6 +545,113 @@ def run_ild(args, rank, world, local):
         }), flush=True)
 
 
+def run_dp(args, w, rank, world, local):
+    """`--mode dp` under torchrun: one data-parallel step per iteration (see the module docstring)."""
+    from hybrid_upcycling_gb300 import _lib, build
+    from hybrid_upcycling_gb300.shard import LibraryCompute, kl_fwd_bwd_sharded
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    torch.distributed.barrier()
+    _lib.load()
+    heads = syn.make_inputs(w, device=dev)  # the same LM heads on every rank (same seed)
+    mine = syn.make_inputs(w, device=dev, seed=w.seed + 7919 * rank) if rank else heads
+    x = {"h_s": mine["h_s"], "h_t": mine["h_t"], "W_s": heads["W_s"], "W_t": heads["W_t"]}
+    del mine
+    stream = torch.cuda.Stream(device=dev)
+    comp = LibraryCompute(timing=True)
+
+    def step(xx):
+        return kl_fwd_bwd_sharded(xx["h_s"], xx["W_s"], xx["h_t"], xx["W_t"], w.tau, w.token_chunk, compute=comp,
+                                  n_total=w.N * world)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step(x)
+    _lib.hylo_kl_sync_status(stream)
+    comp.marks.clear()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id(local)) as clk:
+        with torch.cuda.stream(stream):
+            for e in evs:
+                e[0].record(stream)
+                res = step(x)
+                e[1].record(stream)
+        torch.cuda.synchronize()
+    torch.distributed.barrier()
+    _lib.hylo_kl_sync_status(stream)
+    total_ms = max_over_ranks(evs[0][0].elapsed_time(evs[-1][1]), world, dev)
+    tokens_per_s = whole_job_rate(w.N, world, args.steps, total_ms)
+    tflops = w.flops_exec() * world * args.steps / (total_ms / 1e3) / 1e12
+    marks = list(comp.marks)
+    comp.timing = False
+    fwd_avg = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b, _ in marks])), world, dev)
+    bwd_avg = max_over_ranks(float(np.mean([b.elapsed_time(c) for _, b, c in marks])), world, dev)
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in x.items() if k.startswith("h")}
+        for k in host:
+            host[k].copy_(x[k])
+        slots_in = [{k: torch.empty_like(x[k]) for k in host} for _ in range(2)]
+        slots_out = [{"loss": torch.empty(1, dtype=torch.float64, device=dev),
+                      "kl": torch.empty(w.N, device=dev), "dh": torch.empty(w.N, w.d_s, device=dev),
+                      "dW": torch.empty(w.V, w.d_s, device=dev)} for _ in range(2)]
+
+        def call(xi, xo):  # the heads stay resident; each step's tokens come from host memory
+            r = step({"h_s": xi["h_s"], "h_t": xi["h_t"], "W_s": x["W_s"], "W_t": x["W_t"]})
+            xo["loss"].copy_(r.loss)
+            xo["kl"].copy_(r.kl)
+            xo["dh"].copy_(r.dh_s)
+            xo["dW"].copy_(r.dW_s)
+
+        n_e2e = max(2, min(args.steps, 5))
+        torch.distributed.barrier()
+        ms, d2h = pipelined_e2e(host, slots_in, slots_out, ("loss", "kl", "dh", "dW"), call, n_e2e, stream, dev)
+        torch.distributed.barrier()
+        ms = max_over_ranks(ms, world, dev)
+        e2e = {"value": whole_job_rate(w.N, world, n_e2e, ms), "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+               "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "api": "hybrid_upcycling_gb300.shard.kl_fwd_bwd_sharded (C ABI per rank, NCCL all-reduce of "
+                      "loss and dW_s) with pinned-host token inputs and outputs"}
+        del host, slots_in, slots_out
+    if rank == 0:
+        peaks, peak_src = load_peaks()
+        line = {
+            "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(config_dict(w), parallelism=f"dp{world} (token shards, NCCL all-reduce of loss and dW_s)",
+                           global_batch_tokens=w.N * world),
+            "tflops": tflops, "tflops_unit": "TFLOP/s (4 N V (2 d_s + d_t) executed flops per rank-step, all ranks)",
+            "pct_of_peak": 100.0 * tflops / (NOMINAL_BF16_TFLOPS * world),
+            "peak_source": "NVIDIA dense bf16, 2250 TFLOP/s per GB300 (36 PFLOP/s 2:4-sparse per 8 GPUs / 2 / 8)",
+            "loss": float(res.loss.item()), "cpu_baseline": None, "e2e": e2e,
+            "gpu_launches": launches_per_step(w) * args.steps, "clocks": clk.summary(),
+            "fwd_ms": fwd_avg, "bwd_ms": bwd_avg,
+            "collective_ms": total_ms / args.steps - fwd_avg - bwd_avg,
+        }
+        peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        kernels = [
+            {"kernel": "fused_kl_kernel (+combine, mean)", "ms": fwd_avg, "flops_per_launch": w.flops_fwd(),
+             "tflops": w.flops_fwd() / (fwd_avg / 1e3) / 1e12},
+            {"kernel": "bwd_pipe_kernel", "ms": bwd_avg, "flops_per_launch": w.flops_bwd(),
+             "tflops": w.flops_bwd() / (bwd_avg / 1e3) / 1e12},
+        ]
+        for k in kernels:
+            k["frac"] = k["tflops"] / peak_sus
+        dom = max(kernels, key=lambda k: k["ms"])
+        line["kernels"] = kernels
+        line["roofline"] = {"kernel": dom["kernel"], "bound": "tensor", "achieved": dom["tflops"], "peak": peak_sus,
+                            "unit": "TFLOP/s", "frac": dom["frac"],
+                            "traffic": recorded_traffic(w.name, "hidden" if dom is kernels[1] else "hidden_fwd"),
+                            "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                            "flops_per_launch": dom["flops_per_launch"]}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -559,6 +670,11 @@ def main():
                     help="time hylo_kl_backward_split (G as two bf16 terms) instead of hylo_kl_backward")
     ap.add_argument("--cpu-tokens", type=int, default=256, help="oracle sample size for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=48, help="oracle tokens per reference-arm step")
+    ap.add_argument("--dp-one-rank", action="store_true",
+                    help="run the data-parallel step on a one-rank NCCL group (checks that code path on one GPU)")
+    ap.add_argument("--mode", default="dp", choices=["dp", "replicas"],
+                    help="under torchrun: dp = data-parallel token shards with NCCL all-reduce of loss and dW_s "
+                         "(default); replicas = independent copies of the workload")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 10 if args.impl == "reference" else {"hidden": 10, "logits": 300, "ild": 500}[args.path]
@@ -573,9 +689,14 @@ def main():
         raise SystemExit("bench.py needs a CUDA device")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
+    if world > 1 or args.dp_one_rank:
         import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+        if world == 1:
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            os.environ.setdefault("MASTER_PORT", "29517")
+            dist.init_process_group("nccl", device_id=dev, rank=0, world_size=1)
+        else:
+            dist.init_process_group("nccl", device_id=dev)
     if args.path in ("logits", "ild"):
         if args.path == "logits":
             run_logits(args, w, rank, world, local)
@@ -583,6 +704,10 @@ def main():
             run_ild(args, rank, world, local)
         if world > 1:
             torch.distributed.destroy_process_group()
+        return
+    if (world > 1 and args.mode == "dp") or args.dp_one_rank:
+        run_dp(args, w, rank, world, local)
+        torch.distributed.destroy_process_group()
         return
     from hybrid_upcycling_gb300 import _lib, build
     if rank == 0:

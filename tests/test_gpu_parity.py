@@ -350,6 +350,21 @@ def test_autograd_wrapper(split_g):
     assert abs(loss.item() - float(np.mean(f64(kl)))) < 1e-6
 
 
+def test_functional_fwd_bwd_fp32_gradients_into_caller_buffers():
+    """kl_fwd_bwd: fp32 gradients of grad_scale * loss written into the caller's buffers, equal
+    to the plain C-ABI calls (one workspace shared by the forward and the backward)."""
+    from hybrid_upcycling_gb300.kl import kl_fwd_bwd
+    x = gen(300, 136, 200, 1000, seed=77, w_std=0.1)
+    N, d_s, V = 300, 136, 1000
+    dh = torch.full((N, d_s), float("nan"), device="cuda")
+    dW = torch.full((V, d_s), float("nan"), device="cuda")
+    loss, kl, dh2, dW2 = kl_fwd_bwd(x["h_s"], x["W_s"], x["h_t"], x["W_t"], 0.7, 128, grad_scale=-1.5, dh_s=dh, dW_s=dW)
+    assert dh2 is dh and dW2 is dW and dh.dtype == torch.float32
+    ref = run(x, 0.7, 128, grad_scale=-1.5)
+    assert torch.equal(kl, ref["kl"]) and torch.equal(loss, ref["loss"])
+    assert torch.equal(dh, ref["dh"]) and torch.equal(dW, ref["dW"])
+
+
 # ------------------------------------------------------------------- full workload sizes
 
 def _sample_rows(N, chunk, k, seed):

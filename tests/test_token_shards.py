@@ -5,8 +5,9 @@ concatenated and the shard losses are combined as sum_r N_r loss_r / N.
 This is the data-parallel split of Stage-II distillation (Long-Context Aware Upcycling digest,
 section Experiments: FSDP training): every token's KL and dh_s row depend on its own row alone,
 the mean's 1/N is global, and dW_s = G^T h_s is a sum over tokens. Checked on the oracle
-(sequentially and with a world-size-2 gloo all-reduce on CPU) and through the C ABI on one GPU
-with sequential shards.
+(sequentially and with a world-size-2 gloo all-reduce on CPU), through the package's
+orchestration (hybrid_upcycling_gb300.shard) on two gloo ranks with the oracle as the shard
+compute, and through the C ABI on one GPU (sequential shards; the orchestration on one rank).
 """
 import os
 import socket
@@ -91,6 +92,100 @@ def test_gloo_two_rank_all_reduce_of_shards():
     out = mp.get_context("spawn").Manager().list([1.0, 1.0, 1.0])
     mp.spawn(_worker, args=(2, _free_port(), out), nprocs=2, join=True)
     assert max(out) <= 1e-12, list(out)
+
+
+def _oracle_compute(h_s, W_s, h_t, W_t, tau, token_chunk, grad_scale):
+    """The per-shard computation of hybrid_upcycling_gb300.shard, done by the fp64 oracle (test
+    infrastructure: lets the orchestration run on CPU ranks)."""
+    a = [t.numpy() for t in (h_s, W_s, h_t, W_t)]
+    kl, _, _, loss = orc.kl_forward(*a, tau, token_chunk)
+    dh, dW = orc.kl_backward(*a, tau, token_chunk, grad_scale=grad_scale)
+    return torch.tensor([loss], dtype=torch.float64), torch.from_numpy(kl), torch.from_numpy(dh), torch.from_numpy(dW)
+
+
+def _sharded_worker(rank, world, port, mode, out):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from hybrid_upcycling_gb300.shard import kl_fwd_bwd_sharded, vocab_shard
+    h_s, W_s, h_t, W_t = _problem(seed=9, N=23, d_s=6, d_t=10, V=31)
+    cuts = [0, 9, 23]  # uneven shards: 9 and 14 tokens
+    lo, hi = cuts[rank], cuts[rank + 1]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    res = kl_fwd_bwd_sharded(t(h_s[lo:hi]), t(W_s), t(h_t[lo:hi]), t(W_t), 0.9, token_chunk=4, grad_reduce=mode,
+                             upstream=0.7, compute=_oracle_compute)
+    parts = [None] * world
+    dist.all_gather_object(parts, (res.loss.item(), res.kl.numpy(), res.dh_s.numpy(), res.dW_s.numpy(),
+                                   res.vocab_rows, res.n_total))
+    if rank == 0:
+        kl0, _, _, loss0 = orc.kl_forward(h_s, W_s, h_t, W_t, 0.9)
+        dh0, dW0 = orc.kl_backward(h_s, W_s, h_t, W_t, 0.9, grad_scale=0.7)
+        errs = [max(abs(p[0] - loss0) for p in parts) / loss0,
+                float(np.max(np.abs(np.concatenate([p[1] for p in parts]) - kl0))),
+                float(np.max(np.abs(np.concatenate([p[2] for p in parts]) - dh0)) / np.max(np.abs(dh0)))]
+        if mode == "all_reduce":
+            errs.append(max(float(np.max(np.abs(p[3] - dW0))) for p in parts) / np.max(np.abs(dW0)))
+        else:  # each rank holds its vocabulary shard's rows
+            rows = [p[4] for p in parts]
+            assert rows == [vocab_shard(31, r, world) for r in range(world)], rows
+            errs.append(max(float(np.max(np.abs(p[3] - dW0[p[4][0]:p[4][1]])))
+                            for p in parts) / np.max(np.abs(dW0)))
+            assert sum(r[1] - r[0] for r in rows) == 31
+        assert all(p[5] == 23 for p in parts)
+        for i, e in enumerate(errs):
+            out[i] = e
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("mode", ["all_reduce", "reduce_scatter"])
+def test_sharded_orchestration_two_gloo_ranks(mode):
+    """The package's token-sharded step (hybrid_upcycling_gb300.shard), its per-shard compute done
+    by the oracle: two ranks with 9 and 14 tokens reproduce the unsharded loss, per-token KL, dh_s
+    rows and dW_s (summed, or scattered by vocabulary rows: 31 rows over 2 ranks, padded)."""
+    out = mp.get_context("spawn").Manager().list([1.0] * 4)
+    mp.spawn(_sharded_worker, args=(2, _free_port(), mode, out), nprocs=2, join=True)
+    assert max(out) <= 1e-12, list(out)
+
+
+def test_vocab_shards_cover_the_vocabulary():
+    sys.path.insert(0, ROOT)
+    from hybrid_upcycling_gb300.shard import vocab_shard
+    for V, world in [(31, 2), (128256, 8), (7, 8), (151936, 3)]:
+        rows = [vocab_shard(V, r, world) for r in range(world)]
+        assert rows[0][0] == 0 and rows[-1][1] == V
+        assert all(a[1] == b[0] for a, b in zip(rows[:-1], rows[1:]))
+
+
+@pytest.mark.gpu
+def test_gpu_sharded_step_on_one_rank_matches_the_plain_call():
+    """kl_fwd_bwd_sharded with the library compute on a one-rank NCCL group: the collectives are
+    identities, so the results equal the plain C-ABI calls (same kernels, same inputs)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from hybrid_upcycling_gb300 import _lib, build, synthetic as syn
+    from hybrid_upcycling_gb300.shard import kl_fwd_bwd_sharded
+    build.build()
+    w = syn.WORKLOADS["llama1b_8b_8k"].with_sizes(N=700, V=5000)
+    x = syn.make_inputs(w, device="cuda")
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()))
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda", 0))
+    try:
+        res = kl_fwd_bwd_sharded(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, 512, upstream=0.5)
+        _lib.hylo_kl_sync_status()
+    finally:
+        dist.destroy_process_group()
+    N, f = w.N, dict(dtype=torch.float32, device="cuda")
+    ws = torch.empty(_lib.hylo_kl_workspace_bytes(N, w.d_s, w.d_t, w.V, 512), dtype=torch.uint8, device="cuda")
+    kl, ls, lt, gap = (torch.empty(N, **f) for _ in range(4))
+    loss = torch.empty(1, **f)
+    dh, dW = torch.empty(N, w.d_s, **f), torch.empty(w.V, w.d_s, **f)
+    _lib.hylo_kl_forward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, 512, kl, ls, lt, loss, ws, lse_gap=gap)
+    _lib.hylo_kl_backward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, 512, ls, lt, 0.5, dh, dW, ws, lse_gap=gap)
+    _lib.hylo_kl_sync_status()
+    assert res.n_total == N and res.vocab_rows == (0, w.V)
+    assert abs(res.loss.item() - loss.item()) <= 1e-6 * loss.item()
+    assert torch.equal(res.kl, kl) and torch.equal(res.dh_s, dh) and torch.equal(res.dW_s, dW)
 
 
 @pytest.mark.gpu
