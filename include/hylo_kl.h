@@ -59,11 +59,12 @@ typedef enum {
 
 /* Bytes of device workspace that hylo_kl_forward and hylo_kl_backward need for these sizes:
  * the larger of the forward's per-token partial softmax statistics (6 x 32 x N fp32, O(N)) and
- * the backward's staging of G = dL/dz_s for one block of tokens x vocabulary words (bf16, at
- * most 64 MiB whatever N, V and token_chunk), plus 1280 bytes of counters with which the fused
- * kernels keep the clusters that share LM-head tiles in step. So the extra memory is
- * O(N) + 64 MiB, never O(N * V) or O(token_chunk * V). Returns 0 for invalid sizes.
- * token_chunk <= 0 means 4096. */
+ * the backward's ring of three blocks of G = dL/dz_s (bf16; R tokens x bw words each, with
+ * R = token_chunk rounded up to a multiple of 256, at most 32768, and bw = 64 MiB / (6 R)
+ * rounded down to 256 words: at most 64 MiB in all, whatever N, V and token_chunk), plus 1280
+ * bytes of counters (the forward's pacing words; the backward's work queue and completion
+ * counts). So the extra memory is O(N) + 64 MiB, never O(N * V) or O(token_chunk * V).
+ * Returns 0 for invalid sizes. token_chunk <= 0 means 4096. */
 size_t hylo_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
                                int64_t token_chunk);
 
@@ -85,10 +86,12 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s,
 
 /* Backward: dh_s [N, d_s] and dW_s [V, d_s] (fp32, OVERWRITTEN, not accumulated) for
  * grad_scale * loss, from the lse_s / lse_t (and lse_gap, if not NULL) that hylo_kl_forward
- * wrote for the same inputs. It walks the tokens in blocks of min(token_chunk, N, 32768) rows
- * and the vocabulary in blocks sized so that one block of G (bf16) fits 64 MiB of the
- * workspace; per block it recomputes both logit tiles, forms G, then adds G W_s into dh_s and
- * G^T h_s into dW_s on the tensor cores. Where p_s and p_t of a word agree to within a factor 2^(1/4), G takes the form
+ * wrote for the same inputs. One persistent launch walks the tokens in blocks of R rows and
+ * the vocabulary in blocks of bw words (see hylo_kl_workspace_bytes); per block it recomputes
+ * both logit tiles, forms G into the workspace's ring, and adds G W_s into dh_s and G^T h_s
+ * into dW_s on the tensor cores, in a fixed order (results are deterministic). At most
+ * 2^30 work items (about N x V / 65536 + gradient tiles) per call, else HYLO_ERR_DIM. Where
+ * p_s and p_t of a word agree to within a factor 2^(1/4), G takes the form
  * p_t (2^D - 1), D = log2(p_s / p_t) from the logit difference and lse_gap, which has no
  * cancellation; with lse_gap NULL the gap is lse_s - lse_t, whose rounding bounds the
  * relative accuracy of G at ~1e-6 / |p_s / p_t - 1|. Results match for any token_chunk up
@@ -107,8 +110,8 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s,
  * hylo_kl_backward, with a gradient error of ~1e-5 relative instead of the ~1e-3 that one
  * bf16 rounding of G leaves -- which matters where a token's gradient is dominated by one or
  * two words (near one-hot distributions, or a student that differs from its teacher on few
- * words), where one rounding alone can exceed 2e-3. Costs one more gradient GEMM per chunk
- * and twice the backward's G staging (2 x 64 MiB at most): pass at least
+ * words), where one rounding alone can exceed 2e-3. The gradient products run over both
+ * terms (twice their k-blocks), and the G ring is doubled (2 x 64 MiB at most): pass at least
  * hylo_kl_workspace_bytes_split(...) bytes. (The pages describe no such variant; it is a
  * precision option of this library.) */
 size_t hylo_kl_workspace_bytes_split(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
