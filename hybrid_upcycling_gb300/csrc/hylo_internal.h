@@ -68,6 +68,10 @@ cudaError_t launch_ild(const uint16_t* S, const uint16_t* T, int64_t P, int64_t 
 // to clusters by an atomic counter; completion counters order M(b) after F(b) and after M(b-1)
 // (same output tiles), and F(b) after M(b - kGRing) (same ring slot).
 constexpr int kGRing = 3;
+// Bytes of the G ring (one bf16 term) at most, whatever N, V and token_chunk. 128 MiB holds three
+// blocks of 4096 tokens x 5376 words: fewer, wider vocabulary blocks than a 64 MiB ring, so dh_s
+// is reduce-added half as often (24 instead of 51 times at V = 128256).
+constexpr int64_t kGBlockBytes = int64_t(128) << 20;
 struct BwdPipeParams {
   int N, V, d_s;
   int kb_s, kb_t;   // 64-wide k-blocks of the student / teacher projections

@@ -156,8 +156,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // The backward stages G = dL/dz_s (bf16) in a ring of kGRing blocks of R tokens x bw words:
 // at most kGBlockBytes in all, whatever N, V or token_chunk. R = token_chunk rounded up to a
 // multiple of 256 (at most kMaxBlockTokens, at most N rounded up), so bw is at least
-// kGBlockBytes / (2 kGRing kMaxBlockTokens) = 341 -> 256 words.
-constexpr int64_t kGBlockBytes = int64_t(64) << 20;
+// kGBlockBytes / (2 kGRing kMaxBlockTokens) = 682 -> 512 words.
 constexpr int64_t kMaxBlockTokens = 32768;
 
 int64_t pipe_rows(int64_t N, int64_t token_chunk) {

@@ -60,10 +60,10 @@ typedef enum {
 /* Bytes of device workspace that hylo_kl_forward and hylo_kl_backward need for these sizes:
  * the larger of the forward's per-token partial softmax statistics (6 x 32 x N fp32, O(N)) and
  * the backward's ring of three blocks of G = dL/dz_s (bf16; R tokens x bw words each, with
- * R = token_chunk rounded up to a multiple of 256, at most 32768, and bw = 64 MiB / (6 R)
- * rounded down to 256 words: at most 64 MiB in all, whatever N, V and token_chunk), plus 1280
+ * R = token_chunk rounded up to a multiple of 256, at most 32768, and bw = 128 MiB / (6 R)
+ * rounded down to 256 words: at most 128 MiB in all, whatever N, V and token_chunk), plus 1280
  * bytes of counters (the forward's pacing words; the backward's work queue and completion
- * counts). So the extra memory is O(N) + 64 MiB, never O(N * V) or O(token_chunk * V).
+ * counts). So the extra memory is O(N) + 128 MiB, never O(N * V) or O(token_chunk * V).
  * Returns 0 for invalid sizes. token_chunk <= 0 means 4096. */
 size_t hylo_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
                                int64_t token_chunk);
@@ -111,7 +111,7 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s,
  * bf16 rounding of G leaves -- which matters where a token's gradient is dominated by one or
  * two words (near one-hot distributions, or a student that differs from its teacher on few
  * words), where one rounding alone can exceed 2e-3. The gradient products run over both
- * terms (twice their k-blocks), and the G ring is doubled (2 x 64 MiB at most): pass at least
+ * terms (twice their k-blocks), and the G ring is doubled (2 x 128 MiB at most): pass at least
  * hylo_kl_workspace_bytes_split(...) bytes. (The pages describe no such variant; it is a
  * precision option of this library.) */
 size_t hylo_kl_workspace_bytes_split(int64_t N, int64_t d_s, int64_t d_t, int64_t V,

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 PACE = 1280  # the fused kernels' pacing counters: one 8-byte word per cluster and a switch, to 256 B
-G_RING = 64 << 20  # the backward's G staging: three blocks of tokens x words, at most 64 MiB in all
+G_RING = 128 << 20  # the backward's G staging: three blocks of tokens x words, at most 128 MiB in all
 
 
 def _r256(x):
@@ -47,7 +47,7 @@ def _r256(x):
 
 def _g_ring(N, V, chunk):
     """Bytes of the G ring as documented: 3 blocks of R x bw bf16, R = token_chunk rounded up to
-    256 (at most 32768, at most N rounded up), bw = 64 MiB / (6 R) rounded down to 256 words (at
+    256 (at most 32768, at most N rounded up), bw = 128 MiB / (6 R) rounded down to 256 words (at
     most V rounded up)."""
     c = 4096 if chunk <= 0 else min(chunk, 32768)
     R = min(_r256(c), _r256(N))
@@ -56,13 +56,13 @@ def _g_ring(N, V, chunk):
 
 
 def test_workspace_bytes(lib):
-    """O(N) statistics for the forward, a G ring of at most 64 MiB for the backward: the size
+    """O(N) statistics for the forward, a G ring of at most 128 MiB for the backward: the size
     is bounded independently of V x token_chunk (and never N x V)."""
     N, d_s, d_t, V = 65536, 2048, 4096, 128256
     fwd = 6 * 32 * N * 4
-    # 3 blocks of 4096 tokens x 2560 words of bf16 G = 60 MiB
-    assert _g_ring(N, V, 4096) == 60 << 20
-    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096) == max(fwd, 60 << 20) + PACE
+    # 3 blocks of 4096 tokens x 5376 words of bf16 G = 126 MiB
+    assert _g_ring(N, V, 4096) == 3 * 4096 * 5376 * 2 == 126 << 20
+    assert _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096) == max(fwd, 126 << 20) + PACE
     for n, v, chunk in ((65536, 128256, 4096), (65536, 151936, 1024), (4096, 128256, 4096), (1000, 262144, 4096),
                         (100000, 128256, 100000), (65536, 128256, 65536), (8192, 1 << 20, 8192), (300, 1000, 7),
                         (100, 513, 100000), (64, 100, 4096), (1, 3, 0)):
@@ -72,7 +72,7 @@ def test_workspace_bytes(lib):
         wss = _lib.hylo_kl_workspace_bytes_split(n, d_s, d_t, v, chunk)
         assert wss == max(_r256(6 * 32 * n * 4), 2 * _r256(_g_ring(n, v, chunk))) + PACE
         assert wss <= max(6 * 32 * n * 4, 2 * G_RING) + PACE
-    # at N <= 4096 tokens (one token block) the G staging is still at most 64 MiB, not N x V
+    # at N <= 4096 tokens (one token block) the G staging is still at most 128 MiB, not N x V
     assert _lib.hylo_kl_workspace_bytes(4096, d_s, d_t, V, 4096) < 4096 * V * 2
     assert _lib.hylo_kl_workspace_bytes(8192, 64, 64, 1000, 0) == _lib.hylo_kl_workspace_bytes(8192, 64, 64, 1000, 4096)
     # invalid sizes give 0
@@ -169,7 +169,7 @@ def test_split_workspace_and_rejection(lib):
     N, d_s, d_t, V = 8192, 2048, 4096, 128256
     one = _lib.hylo_kl_workspace_bytes(N, d_s, d_t, V, 4096)
     two = _lib.hylo_kl_workspace_bytes_split(N, d_s, d_t, V, 4096)
-    assert one == (60 << 20) + PACE and two == (120 << 20) + PACE
+    assert one == (126 << 20) + PACE and two == (252 << 20) + PACE
     a = dict(h_s=FAKE, W_s=FAKE, h_t=FAKE, W_t=FAKE, N=16, d_s=64, d_t=128, V=100, tau=1.0, chunk=4096,
              lse_s=FAKE, lse_t=FAKE, gap=None, gs=1.0, dh=FAKE, dW=FAKE, ws=FAKE, stream=None)
     small = _lib.hylo_kl_workspace_bytes(4096, 64, 128, 100000, 4096)

@@ -8,7 +8,8 @@ it everywhere. The gradients are compared on seeded rows the oracle computes one
 vocabulary rows of dW_s (each a sum over all N tokens, from the ORACLE's log-sum-exps, so the
 check is independent of the GPU's statistics). The rows include the first and last ones, the
 edges of the 256-row tiles, of the backward's 4096- and 1024-token blocks and of its
-2560-word vocabulary blocks, and the last (ragged) vocabulary tile. The backward runs with
+vocabulary blocks (the documented width rule: 128 MiB / (6 R) rounded down to 256 words), and
+the last (ragged) vocabulary tile. The backward runs with
 token_chunk 4096 and 1000, so dW_s accumulates over 2 and 8 token blocks.
 
 Tolerances (stated for the fused hidden-state KL): per token |dKL| <= 1e-3 (1 + KL), mean loss
@@ -73,10 +74,16 @@ def token_rows(N, k, seed):
     return np.array(sorted(set(fixed) | set(int(r) for r in rest)))
 
 
+def block_width(R):
+    """Words per vocabulary block of the backward's G ring for R-token blocks."""
+    return (128 << 20) // (6 * R) // 256 * 256
+
+
 def vocab_rows(V, k, seed):
     last_tile = (V - 1) // 256 * 256
-    fixed = {0, 1, V - 1, V - 2, last_tile, last_tile - 1, 255, 256, 2559, 2560, 2561, 5119, 5120}
-    fixed |= {last_tile + 17, (V // 2560) * 2560, (V // 2560) * 2560 - 1}
+    fixed = {0, 1, V - 1, V - 2, last_tile, last_tile - 1, 255, 256, last_tile + 17}
+    for bw in (block_width(4096), block_width(1024)):
+        fixed |= {bw - 1, bw, bw + 1, 2 * bw - 1, 2 * bw, (V // bw) * bw, (V // bw) * bw - 1}
     fixed = {v for v in fixed if 0 <= v < V}
     rng = np.random.default_rng(seed)
     rest = rng.choice(np.setdiff1d(np.arange(V), sorted(fixed)), size=k - len(fixed), replace=False)
