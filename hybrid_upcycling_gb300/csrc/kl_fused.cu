@@ -13,7 +13,8 @@
 // notes, kwkr.cn, section "two-stage training recipe", Stage II).
 //
 // Roles (384 threads per CTA): warp 0 issues the TMA loads, warp 1 of the even CTA owns TMEM
-// and issues the UMMAs for the pair, warps 4..11 are the epilogue (warpgroup 0 gives registers
+// and issues the UMMAs for the pair, warp 2 of the even CTA paces the pair against the other
+// clusters on its vocabulary segment, warps 4..11 are the epilogue (warpgroup 0 gives registers
 // to the two epilogue warpgroups: setmaxnreg 56 / 224). Warp w may read only TMEM lanes
 // 32*(w%4) .. 32*(w%4)+31, so each epilogue thread owns one token row of its CTA's 128-row
 // tile: warps 4..7 take columns 0..127 of the 256-column tile, warps 8..11 columns 128..255.
@@ -52,13 +53,13 @@ struct FusedCfg {
   static constexpr int A_BYTES = kBM * kBK * 2;
   static constexpr int B_BYTES = HB * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
-  // the statistics of one column half handed to the other half at a unit's end
-  static constexpr int EXTRA_BYTES = kStatFields * kBM * 4;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES + EXTRA_BYTES;
+  // as many stages as fit beside the alignment pad and the barriers (7 at BN = 256)
+  static constexpr int STAGES = (232448 - 1024 - 256) / STAGE_BYTES;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
   // full[S], empty[S], tfull[2], tempty[2] (teacher half, student half), merge_full, merge_empty, drain
   static constexpr int NBARS = 2 * STAGES + 4 + 3;
-  static constexpr int SMEM = 1024 + BAR_OFF + NBARS * 8 + 16;
+  // then the TMEM address, the abort flag and the pacing permit
+  static constexpr int SMEM = 1024 + BAR_OFF + NBARS * 8 + 32;
   static_assert(2 * BN == 512 && HALF % 64 == 0 && HB % 8 == 0, "tile shape");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -76,11 +77,14 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsig
 // index k as its peers read the same LM-head tiles in the same order; left alone, clusters
 // drift apart by more tiles than L2 holds and each re-reads the tiles from DRAM (measured on
 // the 64K forward: ~190 GB of DRAM reads per launch). Before loading a vocabulary tile, the
-// even CTA's producer publishes (k, tile) and waits until every peer has reached at least
-// tile - kPaceLead of the same unit index (or finished all its units). The wait is a hint:
-// a producer that waits longer than kPaceWaitNs (a peer not resident, e.g. SMs held by another
-// kernel) sets the switch in slot kMaxClusters and from then on no producer of the launch
-// paces, so a late peer costs at most one such wait, never correctness.
+// even CTA's producer publishes its position (k, tile) and starts the tile only once every
+// peer has reached at least tile - kPaceLead of the same unit index (or finished all its
+// units). The peers' words are polled by a warp of its own (pace_peers), which publishes in
+// shared memory how far the producer may go, so the producer's loads never wait on those
+// global-memory round trips. The wait is a hint: a producer that waits longer than kPaceWaitNs
+// (a peer not resident, e.g. SMs held by another kernel) sets the switch in slot kMaxClusters
+// and from then on no producer of the launch paces, so a late peer costs at most one such
+// wait, never correctness.
 // (Measured: DRAM reads of the 64K forward ~250 -> ~70 GB, 3-7% less time per kernel.)
 // Every word carries the launch's 16-bit epoch in its top bits, so the counters need no
 // clearing between launches: a word from an earlier launch reads as "not started yet", and the
@@ -108,6 +112,93 @@ __device__ __forceinline__ void unit_range(const FusedParams& p, int u, int& row
   vt1 = static_cast<int>((static_cast<long long>(seg + 1) * p.vtiles) / p.nseg);
 }
 
+// The pacing warp of the even CTA. For each of the cluster's units in turn it polls the words of
+// the peers on the same segment (independent loads, eight at a time) and stores in `permit` one
+// more than the furthest position ((unit index << 24) | tile) the producer may start: kPaceLead
+// tiles past the slowest peer, 0 while a peer has not started the unit index, and past the
+// unit's last tile once no peer can hold it back any more. `permit` only grows; it becomes
+// unlimited once pacing is switched off. The warp ends after the last unit, on an abort, or
+// after kPaceGiveUpNs without any peer moving (then it switches pacing off itself).
+constexpr unsigned long long kPaceGiveUpNs = 8 * kPaceWaitNs;
+
+__device__ void pace_peers(const FusedParams& p, int cid, int ncl, volatile unsigned long long* permit,
+                           volatile int* abort_flag) {
+  volatile unsigned long long* prog = p.progress;
+  const unsigned long long ep = static_cast<unsigned long long>(p.epoch) << 48;
+  unsigned long long given = 0;  // the value last stored in permit
+  for (int u = cid, kunit = 0; u < p.units; u += ncl, ++kunit) {
+    int row0, vt0, vt1, seg;
+    unit_range(p, u, row0, vt0, vt1, seg);
+    uint32_t pend[kMaxClusters / 32] = {};  // bit j: cluster j's unit at this index is on this segment
+    for (int j = 0; j < ncl; ++j) {
+      const int uj = j + kunit * ncl;
+      if (j == cid || uj >= p.units) continue;
+      int r_, a_, b_, sj;
+      unit_range(p, uj, r_, a_, b_, sj);
+      if (sj == seg) pend[j >> 5] |= 1u << (j & 31);
+    }
+    const unsigned long long last = (static_cast<unsigned long long>(kunit) << 24) |
+                                    static_cast<unsigned long long>(vt1 - vt0 - 1);
+    uint64_t t_move = globaltimer_ns();
+    unsigned long long seen = 0;  // sum of the pending peers' positions at the last poll
+    while (true) {
+      if (*abort_flag) return;
+      if (prog[kMaxClusters] == ep) {  // pacing was switched off for this launch
+        *permit = ~0ull;
+        return;
+      }
+      unsigned long long allow = last + 1, sum = 0;
+      bool pending = false;
+#pragma unroll 1
+      for (int w = 0; w < kMaxClusters / 32; ++w) {
+        uint32_t bits = pend[w];
+        while (bits != 0u) {
+          int js[8];
+          unsigned long long vs[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            js[i] = bits != 0u ? 32 * w + __ffs(static_cast<int>(bits)) - 1 : -1;
+            bits &= bits - 1u;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) vs[i] = js[i] >= 0 ? prog[js[i]] : 0ull;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (js[i] < 0) continue;
+            const unsigned long long v = vs[i];
+            const unsigned long long lo = v & kPaceLow;
+            if ((v & ~kPaceLow) != ep) {  // not started in this launch: holds everything back
+              allow = 0;
+              pending = true;
+            } else if (lo == kPaceLow || lo + kPaceLead >= last) {  // can no longer hold this unit back
+              pend[w] &= ~(1u << (js[i] & 31));
+            } else {
+              allow = min(allow, lo + kPaceLead + 1);
+              sum += lo + 1;
+              pending = true;
+            }
+          }
+        }
+      }
+      if (allow > given) {
+        given = allow;
+        *permit = allow;
+      }
+      if (!pending) break;
+      const uint64_t now = globaltimer_ns();
+      if (sum != seen) {
+        seen = sum;
+        t_move = now;
+      } else if (now - t_move > kPaceGiveUpNs) {  // no peer moved: give up pacing for the launch
+        prog[kMaxClusters] = ep;
+        *permit = ~0ull;
+        return;
+      }
+      __nanosleep(200);
+    }
+  }
+}
+
 template <int BN_>
 __global__ void __launch_bounds__(kThreads, 1)
 fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant__ CUtensorMap tm_Ws,
@@ -119,7 +210,6 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
   constexpr int HALF = C::HALF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* extra = smem + C::STAGES * C::STAGE_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);  // used in the even CTA
   uint64_t* empty = full + C::STAGES;       // both CTAs: stage free (UMMAs done reading it)
   uint64_t* tfull = empty + C::STAGES;      // both CTAs: TMEM half h (0 teacher, 1 student) complete
@@ -129,6 +219,7 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
   uint64_t* drain = merge_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile unsigned long long* permit = reinterpret_cast<volatile unsigned long long*>(drain + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -149,6 +240,7 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
     mbar_init(merge_empty, kEpiWarps / 2);
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *permit = 0;
     fence_mbar_init();
   }
   if (threadIdx.x == 32) {
@@ -181,68 +273,27 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
       uint32_t phase = 0;
       uint32_t armed = 0;  // bit s: stage s has been armed at least once (even CTA)
       bool ok = true;
-      for (int u = cid; ok && u < p.units; u += ncl) {
+      bool pace = p.progress != nullptr && rank == 0;
+      const unsigned long long ep = static_cast<unsigned long long>(p.epoch) << 48;
+      for (int u = cid, kunit = 0; ok && u < p.units; u += ncl, ++kunit) {
         int row0, vt0, vt1, seg;
         unit_range(p, u, row0, vt0, vt1, seg);
         const int arow = row0 + my_rows;
-        const bool pace = p.progress != nullptr && rank == 0;
-        const unsigned long long ep = static_cast<unsigned long long>(p.epoch) << 48;
-        const unsigned long long kunit = static_cast<unsigned long long>((u - cid) / ncl);
-        uint32_t peers[kMaxClusters / 32] = {};  // bit j: cluster j's unit at index kunit is on this segment
-        if (pace) {
-          for (int j = 0; j < ncl; ++j) {
-            const int uj = j + static_cast<int>(kunit) * ncl;
-            if (j == cid || uj >= p.units) continue;
-            int r_, a_, b_, sj;
-            unit_range(p, uj, r_, a_, b_, sj);
-            if (sj == seg) peers[j >> 5] |= 1u << (j & 31);
-          }
-        }
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           const int brow = vt * BN + static_cast<int>(rank) * HB;
           if (pace) {
-            // One poll reads every peer that is still behind with independent loads (eight at a
-            // time), so a check costs about one round trip to L2 rather than one per peer.
-            volatile unsigned long long* prog = p.progress;
-            const unsigned long long mine = (kunit << 24) | static_cast<unsigned long long>(vt - vt0);
-            prog[cid] = ep | mine;
-            const uint64_t t0 = globaltimer_ns();
-            uint32_t pend[kMaxClusters / 32];
-#pragma unroll
-            for (int w = 0; w < kMaxClusters / 32; ++w) pend[w] = peers[w];
-            while (true) {
-              if (prog[kMaxClusters] == ep) break;  // pacing was given up for this launch
-              bool behind = false;
-#pragma unroll 1
-              for (int w = 0; w < kMaxClusters / 32; ++w) {
-                uint32_t bits = pend[w];
-                while (bits != 0u) {
-                  int js[8];
-                  unsigned long long vs[8];
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) {
-                    js[i] = bits != 0u ? 32 * w + __ffs(static_cast<int>(bits)) - 1 : -1;
-                    bits &= bits - 1u;
-                  }
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) vs[i] = js[i] >= 0 ? prog[js[i]] : 0ull;
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) {
-                    if (js[i] < 0) continue;
-                    const unsigned long long v = vs[i];
-                    const unsigned long long lo = v & kPaceLow;
-                    // a peer of this launch (its epoch tag) that finished or is at most kPaceLead tiles behind
-                    if ((v & ~kPaceLow) == ep && (lo == kPaceLow || lo + kPaceLead >= mine))
-                      pend[w] &= ~(1u << (js[i] & 31));
-                    else
-                      behind = true;
-                  }
+            const unsigned long long mine =
+                (static_cast<unsigned long long>(kunit) << 24) | static_cast<unsigned long long>(vt - vt0);
+            reinterpret_cast<volatile unsigned long long*>(p.progress)[cid] = ep | mine;
+            if (*permit <= mine) {
+              const uint64_t t0 = globaltimer_ns();
+              while (*permit <= mine) {
+                if (*abort_flag) break;
+                if (globaltimer_ns() - t0 > kPaceWaitNs) {  // give up pacing for the whole launch
+                  reinterpret_cast<volatile unsigned long long*>(p.progress)[kMaxClusters] = ep;
+                  pace = false;
+                  break;
                 }
-              }
-              if (!behind) break;
-              if (globaltimer_ns() - t0 > kPaceWaitNs) {  // give up pacing for the whole launch
-                prog[kMaxClusters] = ep;
-                break;
               }
             }
           }
@@ -339,6 +390,9 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
         drain_wait(drain, 0, 100000000ull);
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ pacing (even CTA)
+    if (lane == 0 && rank == 0 && p.progress != nullptr) pace_peers(p, cid, ncl, permit, abort_flag);
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     setmaxnreg_inc<kRegsEpilogue>();
@@ -347,7 +401,6 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
     const int h = e >> 2;           // column half of the tile: [h*HALF, h*HALF + HALF)
     const int row = q * 32 + lane;  // token row inside this CTA's 128 rows
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(h * HALF);
-    float* merge = reinterpret_cast<float*>(extra);  // [kStatFields][128]
     int lt = 0, lu = 0;
     bool ok = true;
     for (int u = cid; ok && u < p.units; u += ncl, ++lu) {
@@ -396,32 +449,41 @@ fused_kl_kernel(const __grid_constant__ CUtensorMap tm_hs, const __grid_constant
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(tempty + 1), 0));
       }
       if (!ok) break;
-      // column half 1 hands its statistics to half 0, which merges and writes them
+      // Column half 1 hands its statistics to half 0, which merges them and writes the result.
+      // The hand-off goes through the unit's own slot of the partial statistics (each unit, a
+      // (pair tile, segment), owns its slots), read back by the same CTA: no shared memory, which
+      // leaves room for a seventh operand stage.
       const uint32_t par = static_cast<uint32_t>(lu & 1);
+      const size_t NS = static_cast<size_t>(p.N);
+      const size_t fs = static_cast<size_t>(p.nseg) * NS;  // stride between fields
+      float* base = p.part + static_cast<size_t>(seg) * NS + token;
       if (h == 1) {
         bool w = wait_bounded(merge_empty, par ^ 1u, abort_flag, p.ctl, 5);
         if (!__all_sync(0xffffffffu, w)) break;
-        merge[0 * kBM + row] = rs.mt;
-        merge[1 * kBM + row] = rs.st;
-        merge[2 * kBM + row] = rs.ms;
-        merge[3 * kBM + row] = rs.ss;
-        merge[4 * kBM + row] = rs.a;
-        merge[5 * kBM + row] = rs.far ? -1.f : rs.cc;  // cc >= 0 otherwise, so -1 marks "far"
+        if (token < p.N) {
+          base[0 * fs] = rs.mt;
+          base[1 * fs] = rs.st;
+          base[2 * fs] = rs.ms;
+          base[3 * fs] = rs.ss;
+          base[4 * fs] = rs.a;
+          base[5 * fs] = rs.far ? -1.f : rs.cc;  // cc >= 0 otherwise, so -1 marks "far"
+        }
+        __threadfence_block();
         __syncwarp();
         if (lane == 0) mbar_arrive(merge_full);
       } else {
         bool w = wait_bounded(merge_full, par, abort_flag, p.ctl, 6);
         if (!__all_sync(0xffffffffu, w)) break;
-        const float occ = merge[5 * kBM + row];
-        const RowStats o{merge[0 * kBM + row], merge[1 * kBM + row], merge[2 * kBM + row],
-                         merge[3 * kBM + row], merge[4 * kBM + row], occ < 0.f ? 0.f : occ, occ < 0.f};
+        RowStats o{-INFINITY, 0.f, -INFINITY, 0.f, 0.f, 0.f, false};
+        if (token < p.N) {
+          const float occ = base[5 * fs];
+          o = RowStats{base[0 * fs], base[1 * fs], base[2 * fs], base[3 * fs], base[4 * fs],
+                       occ < 0.f ? 0.f : occ, occ < 0.f};
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(merge_empty);
-        merge_stats(rs, o, p.c);
         if (token < p.N) {
-          const size_t NS = static_cast<size_t>(p.N);
-          float* base = p.part + static_cast<size_t>(seg) * NS + token;
-          const size_t fs = static_cast<size_t>(p.nseg) * NS;  // stride between fields
+          merge_stats(rs, o, p.c);
           base[0 * fs] = rs.mt;
           base[1 * fs] = rs.st;
           base[2 * fs] = rs.ms;
