@@ -157,7 +157,8 @@ hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16_t* W_s,
  * not NULL, the gradient of grad_scale * loss with respect to z_s,
  * dz_s[n, v] = grad_scale * (p_s - p_t) / (tau N), as bf16 in an [N, ld] buffer (columns
  * v >= V untouched). One kernel; reads each logit once for the statistics and, with a
- * gradient, once more from L2. Needs no workspace. */
+ * gradient, once more for dz_s (from DRAM: between a row's two passes the GPU streams more
+ * than L2 holds). Needs no workspace. */
 hylo_status hylo_fused_kl_logits(const uint16_t* z_s, const uint16_t* z_t,
                                  int64_t N, int64_t V, int64_t ld,
                                  float tau, float grad_scale,
