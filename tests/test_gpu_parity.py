@@ -510,3 +510,39 @@ def test_results_identical_when_clusters_start_late():
     torch.cuda.synchronize()
     for k in ("kl", "lse_s", "lse_t", "loss", "gap", "dh", "dW"):
         assert torch.equal(a[k], b[k]), k
+
+
+def test_index_range_beyond_2_31_elements():
+    """N = 2^21 + 37 tokens of d_s = 1024: h_s holds more than 2^31 elements (4.3 GB, byte
+    offsets past 2^32), dh_s more than 2^31 fp32. The token rows repeat a period of U = 1024
+    distinct rows, so the fp64 oracle evaluates the U distinct rows once: each token's KL and
+    log-sum-exps are its row's, G carries the global N, dW_s = sum_u mult(u) G_u^T h_u. Every
+    token's KL, the mean loss, dW_s, and dh_s on rows spread over the whole range (around the
+    2^31-element offset and at the end) against it; tokens with the same inputs get the same
+    bits."""
+    U, N, d_s, d_t, V, tau = 1024, (1 << 21) + 37, 1024, 1536, 300, 1.0
+    xu = gen(U, d_s, d_t, V, seed=55)
+    reps = -(-N // U)
+    x = {"h_s": xu["h_s"].repeat(reps, 1)[:N].contiguous(), "h_t": xu["h_t"].repeat(reps, 1)[:N].contiguous(),
+         "W_s": xu["W_s"], "W_t": xu["W_t"]}
+    assert x["h_s"].numel() > 2 ** 31
+    g = run(x, tau)
+    hu, Ws, htu, Wt = (f64(xu[k]) for k in ("h_s", "W_s", "h_t", "W_t"))
+    kl_u, ls_u, lt_u, _ = orc.kl_forward(hu, Ws, htu, Wt, tau)
+    mult = np.bincount(np.arange(N) % U, minlength=U).astype(np.float64)
+    G_u = orc.kl_grad_logits(hu, Ws, htu, Wt, tau, 1.0, N)
+    dW = (G_u * mult[:, None]).T @ hu
+    loss = float(np.dot(mult, kl_u) / N)
+    idx = torch.arange(N, device="cuda") % U
+    kl_ref = torch.from_numpy(kl_u).cuda()[idx]
+    assert torch.all((g["kl"].double() - kl_ref).abs() <= TOL_KL * (1 + kl_ref)).item()
+    assert abs(g["loss"].item() - loss) <= TOL_LOSS * loss
+    assert frob_rel(f64(g["dW"]), dW) <= TOL_GRAD, frob_rel(f64(g["dW"]), dW)
+    rows = np.array(sorted({0, 1, U, (1 << 21) - 1, 1 << 21, (1 << 21) + 1, N - 1, N - 2}
+                           | set(np.random.default_rng(7).choice(N, 200, replace=False).tolist())))
+    dh_rows = f64(g["dh"][torch.from_numpy(rows).cuda()])
+    dh_ref = G_u[rows % U] @ Ws
+    assert frob_rel(dh_rows, dh_ref) <= TOL_GRAD, frob_rel(dh_rows, dh_ref)
+    first = torch.from_numpy(rows % U).cuda()
+    assert torch.equal(g["dh"][torch.from_numpy(rows).cuda()], g["dh"][first])
+    assert torch.equal(g["kl"][torch.from_numpy(rows).cuda()], g["kl"][first])
