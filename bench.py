@@ -606,7 +606,7 @@ def run_dp(args, w, rank, world, local):
             xo["dh"].copy_(r.dh_s)
             xo["dW"].copy_(r.dW_s)
 
-        n_e2e = max(2, min(args.steps, 5))
+        n_e2e = max(2, min(args.steps, 10))
         torch.distributed.barrier()
         ms, d2h = pipelined_e2e(host, slots_in, slots_out, ("loss", "kl", "dh", "dW"), call, n_e2e, stream, dev)
         torch.distributed.barrier()
@@ -778,7 +778,7 @@ def main():
         # one shared workspace (and flags); fresh output buffers for the second slot
         bo = [b, {k: (torch.empty_like(v) if torch.is_tensor(v) and k != "ws" else v) for k, v in b.items()}]
         h2d = sum(v.numel() * v.element_size() for v in host.values())
-        e2e_steps = max(2, min(args.steps, 5))
+        e2e_steps = max(2, min(args.steps, 10))  # fill and drain (first upload, last download) amortised over the steps
         barrier()
         e2e_ms, d2h = pipelined_e2e(host, xd, bo, ("kl", "loss", "dh", "dW"),
                                     lambda xi, xo: step(w, xi, xo, stream), e2e_steps, stream, dev)
