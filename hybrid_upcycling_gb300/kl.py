@@ -1,11 +1,13 @@
-"""User-facing PyTorch wrappers of the fused hidden-state KL loss.
+"""User-facing PyTorch wrappers of the fused hidden-state KL loss and its two siblings.
 
 ``fused_hidden_state_kl(h_s, W_s, h_t, W_t, tau)`` is an autograd function: it returns the mean
 KL(p_t || p_s) over all tokens (and the per-token values), and its backward gives d/dh_s and
 d/dW_s in the inputs' dtype. ``kl_fwd_bwd(...)`` runs forward and backward in one call and
 returns fp32 gradients (optionally into caller buffers), for trainers that keep fp32 gradient
-accumulators. Both run entirely in the sm_103a kernels of libhylo_kl.so through the C ABI;
-PyTorch only allocates the outputs and the workspace. The teacher inputs (h_t, W_t) receive no
+accumulators. ``fused_logits_kl(z_s, z_t, tau)`` is the same loss on precomputed logits and
+``ild_loss(S, T)`` the Stage-I layer-alignment loss, both autograd functions whose gradient is
+formed in the forward launch. All run entirely in the sm_103a kernels of libhylo_kl.so through
+the C ABI; PyTorch only allocates the outputs and the workspace. The teacher inputs receive no
 gradient.
 """
 from __future__ import annotations
@@ -104,3 +106,89 @@ def kl_fwd_bwd(h_s, W_s, h_t, W_t, tau: float = 1.0, token_chunk: int = 4096, gr
     dW_s = torch.empty(V, d_s, **f) if dW_s is None else dW_s
     _backward(h_s, W_s, h_t, W_t, tau, token_chunk, lse_s, lse_t, gap, ws, grad_scale, dh_s, dW_s, split_g)
     return loss, kl, dh_s, dW_s
+
+
+def _logits_rows(z: torch.Tensor) -> torch.Tensor:
+    """z itself if its rows meet the C ABI's layout (unit column stride, row stride a multiple
+    of 8 elements), else a copy into rows padded to a multiple of 8 (returned as a [N, V] view)."""
+    N, V = z.shape
+    if z.stride(1) == 1 and z.stride(0) >= V and z.stride(0) % 8 == 0:
+        return z
+    ld = (V + 7) // 8 * 8
+    buf = torch.empty(N, ld, dtype=z.dtype, device=z.device)
+    buf[:, :V] = z
+    return buf[:, :V]
+
+
+class FusedLogitsKL(torch.autograd.Function):
+    """Mean KL(softmax(z_t / tau) || softmax(z_s / tau)) over the rows of precomputed bf16
+    logits [N, V], through hylo_fused_kl_logits. The gradient with respect to z_s is formed in
+    the same launch as the loss (when z_s needs one) and scaled by the upstream gradient in the
+    backward; z_t (the teacher) receives none."""
+
+    @staticmethod
+    def forward(ctx, z_s, z_t, tau: float = 1.0):
+        if z_s.shape != z_t.shape or z_s.dtype != torch.bfloat16 or z_t.dtype != torch.bfloat16:
+            raise ValueError("z_s and z_t must be bfloat16 tensors of the same [N, V] shape")
+        zs, zt = _logits_rows(z_s), _logits_rows(z_t)
+        if zs.stride(0) != zt.stride(0):  # the ABI takes one row stride for both
+            zs, zt = _logits_rows(zs.contiguous()), _logits_rows(zt.contiguous())
+        N, V = zs.shape
+        f = dict(dtype=torch.float32, device=zs.device)
+        kl, lse_s, lse_t = (torch.empty(N, **f) for _ in range(3))
+        loss = torch.empty(1, **f)
+        dz = None
+        if ctx.needs_input_grad[0]:
+            dz = torch.empty(N, zs.stride(0), dtype=torch.bfloat16, device=zs.device)[:, :V]
+        _lib.hylo_fused_kl_logits(zs, zt, tau, 1.0, kl, lse_s, lse_t, loss, dz)
+        ctx.save_for_backward(dz if dz is not None else torch.empty(0, device=zs.device))
+        ctx.has_dz = dz is not None
+        ctx.mark_non_differentiable(kl)
+        return loss[0], kl
+
+    @staticmethod
+    def backward(ctx, g_loss, g_kl):
+        (dz,) = ctx.saved_tensors
+        if not ctx.has_dz or g_loss is None:
+            return None, None, None
+        return dz * g_loss.to(torch.float32), None, None
+
+
+def fused_logits_kl(z_s, z_t, tau: float = 1.0):
+    """Mean KL(p_t || p_s) over rows of bf16 logits z_s, z_t [N, V], and the per-row KL; the
+    student logits z_s receive the gradient (bf16)."""
+    return FusedLogitsKL.apply(z_s, z_t, tau)
+
+
+class ILDLoss(torch.autograd.Function):
+    """Stage-I alignment loss sum_p mean_n ||S[p, n] - T[p, n]||_2 over stacked bf16 tensors
+    [P, N, d], through hylo_ild_loss. The gradient with respect to S is formed in the same
+    launch (when S needs one) and scaled by the upstream gradient in the backward; T (the
+    teacher) receives none."""
+
+    @staticmethod
+    def forward(ctx, S, T):
+        S, T = S.contiguous(), T.contiguous()
+        P, N, d = S.shape
+        f = dict(dtype=torch.float32, device=S.device)
+        norms = torch.empty(P, N, **f)
+        loss = torch.empty(1, **f)
+        dS = torch.empty_like(S) if ctx.needs_input_grad[0] else None
+        _lib.hylo_ild_loss(S, T, 1.0, norms, loss, dS)
+        ctx.save_for_backward(dS if dS is not None else torch.empty(0, device=S.device))
+        ctx.has_dS = dS is not None
+        ctx.mark_non_differentiable(norms)
+        return loss[0], norms
+
+    @staticmethod
+    def backward(ctx, g_loss, g_norms):
+        (dS,) = ctx.saved_tensors
+        if not ctx.has_dS or g_loss is None:
+            return None, None
+        return dS * g_loss.to(torch.float32), None
+
+
+def ild_loss(S, T):
+    """Stage-I ILD loss of student S against teacher T ([P, N, d] bf16) and the per-row norms
+    [P, N]; S receives the gradient (bf16)."""
+    return ILDLoss.apply(S, T)

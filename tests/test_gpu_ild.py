@@ -94,3 +94,24 @@ def test_stage1_shape_sampled():
     rg /= N  # the oracle above averaged over 1 token per entry
     err = np.linalg.norm(f64(dS[ps, ns]) - rg[:, 0, :]) / np.linalg.norm(rg)
     assert err <= 2e-3, err
+
+
+def test_autograd_wrapper_matches_oracle():
+    """kl.ild_loss as an autograd function: loss, norms and S.grad through loss.backward()
+    (upstream 1: the kernel's single bf16 rounding), a second backward with upstream 3 (one
+    more bf16 rounding of the scaled gradient, so twice the bound), and no gradient for T."""
+    from hybrid_upcycling_gb300.kl import ild_loss
+    S, T = states(3, 70, 1032, seed=61)
+    norms_r, loss_r, G = orc.ild_loss(f64(S), f64(T))
+    Sg = S.clone().requires_grad_(True)
+    loss, norms = ild_loss(Sg, T)
+    loss.backward()
+    assert abs(loss.item() - loss_r) <= 1e-5 * loss_r
+    assert np.all(np.abs(f64(norms) - norms_r) <= 1e-5 * norms_r)
+    assert Sg.grad.dtype == torch.bfloat16 and Sg.grad.shape == S.shape
+    assert np.linalg.norm(f64(Sg.grad) - G) / np.linalg.norm(G) <= 2e-3
+    Sg.grad = None
+    loss, _ = ild_loss(Sg, T)
+    (3.0 * loss).backward()
+    assert np.linalg.norm(f64(Sg.grad) - 3 * G) / np.linalg.norm(3 * G) <= 4e-3
+    assert T.grad is None

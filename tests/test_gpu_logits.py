@@ -168,3 +168,25 @@ def test_full_size_logits_sampled():
     err = np.linalg.norm(f64(g["dz"][rows]) - G) / np.linalg.norm(G)
     print(f"logits full size: kl max err {np.max(np.abs(gk - kl)):.2e}, dz rows rel {err:.2e}")
     assert err <= TOL_GRAD
+
+
+def test_autograd_wrapper_matches_oracle():
+    """kl.fused_logits_kl as an autograd function on logits whose rows are not a multiple of 8
+    (the wrapper pads them): loss, per-row KL and z_s.grad through loss.backward() (upstream 1:
+    the kernel's single bf16 rounding), then upstream 2.5 (one more bf16 rounding, twice the
+    bound); no gradient for z_t."""
+    from hybrid_upcycling_gb300.kl import fused_logits_kl
+    z_s, z_t = logits(130, 1001, seed=90)
+    kl_r, _, _, loss_r, G = orc.kl_from_logits(f64(z_s), f64(z_t), 1.3)
+    zs = z_s.clone().requires_grad_(True)
+    loss, kl = fused_logits_kl(zs, z_t, 1.3)
+    loss.backward()
+    assert abs(loss.item() - loss_r) <= TOL_LOSS * loss_r
+    assert np.all(np.abs(f64(kl) - kl_r) <= TOL_KL * (1 + kl_r))
+    assert zs.grad.dtype == torch.bfloat16 and zs.grad.shape == z_s.shape
+    assert np.linalg.norm(f64(zs.grad) - G) / np.linalg.norm(G) <= TOL_GRAD
+    zs.grad = None
+    loss, _ = fused_logits_kl(zs, z_t, 1.3)
+    (2.5 * loss).backward()
+    assert np.linalg.norm(f64(zs.grad) - 2.5 * G) / np.linalg.norm(2.5 * G) <= 2 * TOL_GRAD
+    assert z_t.grad is None
