@@ -546,3 +546,11 @@ def test_index_range_beyond_2_31_elements():
     first = torch.from_numpy(rows % U).cuda()
     assert torch.equal(g["dh"][torch.from_numpy(rows).cuda()], g["dh"][first])
     assert torch.equal(g["kl"][torch.from_numpy(rows).cuda()], g["kl"][first])
+
+
+def test_vocabulary_of_a_million_words():
+    """V = 1,000,003 (ragged): 3907 vocabulary tiles in the forward, 87296-word blocks in the
+    backward (the G ring's width rule at 256-token blocks) with a partial last block; every
+    output against the dense oracle."""
+    x = gen(200, 64, 96, 1_000_003, seed=77, w_std=0.1)
+    check_dense(x, 1.0, 4096, 1.0, loss_abs=1e-7)
