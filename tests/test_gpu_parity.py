@@ -273,6 +273,22 @@ def test_token_chunk_invariance_and_determinism():
     assert frob_rel(f64(b["dW"]), f64(a["dW"])) < 1e-6
 
 
+@pytest.mark.parametrize("chunk", [0, 1, 600, 10 ** 9])
+def test_token_chunk_extremes(chunk):
+    """token_chunk 0 means 4096 (bit-identical); 1 is rounded up to one 256-row block; N itself
+    is one block; 10^9 is capped (at 32768 rows, then at N rounded up to 256). The forward never
+    depends on the chunk; the gradients agree to fp32 summation order."""
+    x = gen(600, 128, 256, 5000, seed=3, w_std=0.08)
+    a = run(x, 1.0, token_chunk=4096)
+    b = run(x, 1.0, token_chunk=chunk)
+    for k in ("kl", "lse_s", "lse_t", "loss"):
+        assert torch.equal(a[k], b[k]), k
+    if chunk == 0:
+        assert torch.equal(a["dh"], b["dh"]) and torch.equal(a["dW"], b["dW"])
+    assert frob_rel(f64(b["dh"]), f64(a["dh"])) < 1e-6
+    assert frob_rel(f64(b["dW"]), f64(a["dW"])) < 1e-6
+
+
 def test_runs_on_a_side_stream():
     x = gen(256, 64, 128, 700, seed=11)
     ref = run(x, 1.0)
