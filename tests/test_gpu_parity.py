@@ -570,3 +570,11 @@ def test_vocabulary_of_a_million_words():
     output against the dense oracle."""
     x = gen(200, 64, 96, 1_000_003, seed=77, w_std=0.1)
     check_dense(x, 1.0, 4096, 1.0, loss_abs=1e-7)
+
+
+@pytest.mark.parametrize("d_s,d_t", [(520, 8), (264, 72)])
+def test_student_wider_than_teacher(d_s, d_t):
+    """d_t < d_s (the teacher's K-blocks are the fewer, one of them ragged at d_t = 8 or 72);
+    every output against the dense oracle."""
+    x = gen(333, d_s, d_t, 2100, seed=d_s + d_t, w_std=0.1)
+    check_dense(x, 1.0, 128, 1.0, loss_abs=1e-7)
