@@ -10,16 +10,17 @@
 // next-token distributions (HyLo-Llama-8MLA8GDN-8K-SFT reading notes, Stage II).
 //
 // A cluster of kSplit CTAs works on one row at a time, each CTA on a contiguous column slice,
-// and the clusters walk the rows. In each CTA a producer warp streams 8192-column chunks of
-// its slice with 1-D bulk TMA copies into a 3-stage shared-memory ring; 8 consumer warps each
-// take 32 columns of a chunk per thread (four 16-byte vectors, interleaved so every shared
-// load of a warp is one contiguous 512-byte run). Pass 1 folds the slice into running
+// and the clusters walk the rows. In each CTA a producer warp streams 6144-column chunks of
+// its slice with 1-D bulk TMA copies into a 4-stage shared-memory ring; 12 consumer warps
+// (three per scheduler) each take 16 columns of a chunk per thread (two 16-byte vectors,
+// interleaved so every shared load of a warp is one contiguous 512-byte run). (With 8 warps of
+// 32 columns and 8192-column chunks: 12.94 against 12.62 ms for 65536 x 128256.) Pass 1 folds the slice into running
 // statistics (shared with the hidden-state kernel); pass 2 (gradient requested) streams the
 // slice again and stores dz_s. Each stage carries pass 1 of row k together with pass 2 of
 // row k - kLag, so the HBM-bound and the exponential-bound halves of the work overlap.
 //
 // No warp waits for a row's statistics: at the end of its pass 1 every warp deposits its
-// partial and moves on; one warp, rotating with the row (k mod 8), merges the eight partials,
+// partial and moves on; one warp, rotating with the row (k mod 12), merges the partials,
 // exchanges the slice result with the other CTAs of the cluster through DSMEM (stores into
 // every CTA's shared memory, release-arrive on its barrier; each CTA merges the kSplit
 // partials in rank order, so all hold the same bits), forms lse, KL and the gap in fp32 and
@@ -31,7 +32,9 @@
 //
 // HBM: pass 2 re-reads the row from DRAM, not L2 (ncu on 8192 x 128256: L2 hit rate ~0%,
 // DRAM at 80% of its peak, ~10 B moved per element against 6 algorithmic): between a row's two
-// passes every SM streams more than a whole row, >100 MB across the GPU. Splitting rows over a
+// passes every SM streams more than a whole row, >100 MB across the GPU. The consumers are
+// about as slow: with pass 2 served from L2 by construction (a timing probe) the launch is only
+// 2-4% faster, so the two limits coincide. Splitting rows over a
 // cluster shortens that distance but measured slower on GB300 (8192 x 128256, one launch:
 // kSplit 1: 1.66 ms, 2: 1.74, 4: 2.18, 8: 3.96): 4- and 8-CTA clusters leave 8 and 32 SMs
 // idle (36 and 15 clusters resident), the per-row exchange adds latency that the 3-stage ring
@@ -43,13 +46,14 @@
 namespace hylo {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 12;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one producer warp
-constexpr int kChunk = 8192;                          // columns per stage
+constexpr int kChunk = 6144;                          // columns per stage
 constexpr int kChunkBytes = kChunk * 2;               // per tensor
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kStageBytes = 4 * kChunkBytes;  // pass-1 (z_t, z_s) and pass-2 (z_t, z_s) chunks
-constexpr int kVecPerThread = 4;              // 4 x 8 columns = 32 per thread per chunk
+constexpr int kVecPerThread = 2;              // 2 x 8 columns = 16 per thread per chunk
+constexpr int kCols = 8 * kVecPerThread;
 static_assert(kConsumerWarps * 32 * kVecPerThread * 8 == kChunk, "chunk split");
 constexpr int kTail = 2048;                   // barriers and exchange slots
 constexpr int kSmem = 1024 + kStages * kStageBytes + kTail;
@@ -294,19 +298,19 @@ __global__ void __launch_bounds__(kThreads, 1) kl_logits_kernel(const LogitsPara
           }
         }
         if (p1) {  // pass 1 of row n1: fold
-          float zt[32], zs[32];
+          float zt[kCols], zs[kCols];
 #pragma unroll
           for (int i = 0; i < kVecPerThread; ++i) {
             unpack_bf16x8(reinterpret_cast<const uint4*>(st)[vec[i]], zt + 8 * i);
             unpack_bf16x8(reinterpret_cast<const uint4*>(st + kChunkBytes)[vec[i]], zs + 8 * i);
           }
           if (valid == 0xffffffffu)
-            fold_chunk<false>(rs, zt, zs, valid, p.c, p.inv_tau);
+            fold_chunk<false, kCols>(rs, zt, zs, valid, p.c, p.inv_tau);
           else if (valid != 0)
-            fold_chunk<true>(rs, zt, zs, valid, p.c, p.inv_tau);
+            fold_chunk<true, kCols>(rs, zt, zs, valid, p.c, p.inv_tau);
         }
         if (p2) {  // pass 2 of row n2: dz_s = gscale (p_s - p_t)
-          float zt[32], zs[32];
+          float zt[kCols], zs[kCols];
 #pragma unroll
           for (int i = 0; i < kVecPerThread; ++i) {
             unpack_bf16x8(reinterpret_cast<const uint4*>(st + 2 * kChunkBytes)[vec[i]], zt + 8 * i);
@@ -314,9 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1) kl_logits_kernel(const LogitsPara
           }
           const float2 c2 = make_float2(p.c, p.c), gs2 = make_float2(p.gscale, p.gscale);
           const float2 nbt = make_float2(-bt, -bt), nbs = make_float2(-bs, -bs), ngl2 = make_float2(ngl, ngl);
-          uint32_t pk[16];
+          uint32_t pk[kCols / 2];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < kCols / 2; ++j) {
             const float2 g = __fmul2_rn(prob_diff2(make_float2(zt[2 * j], zt[2 * j + 1]),
                                                    make_float2(zs[2 * j], zs[2 * j + 1]), c2, nbt, nbs, ngl2),
                                         gs2);

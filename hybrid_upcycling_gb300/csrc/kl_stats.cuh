@@ -47,12 +47,12 @@ __device__ __forceinline__ float2 ex2_approx2(float2 x) { return make_float2(ex2
 // e_t (exp(-d) - 1 + d) = e_s K - e_t + e_t d with K = exp((m_s - m_t)/tau), which uses no
 // extra exponential. K is clamped to stay finite; if the clamp engages the row is marked far.
 // zt_in, zs_in: 32 consecutive values each (register arrays indexed with compile-time offsets).
-template <bool MASKED>
+template <bool MASKED, int W = 32>
 __device__ __forceinline__ void fold_chunk(RowStats& r, const float* zt_in, const float* zs_in, uint32_t valid,
                                            float c, float inv_tau) {
   float cmt = -INFINITY, cms = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
+  for (int j = 0; j < W; ++j) {
     if (!MASKED || ((valid >> j) & 1u)) {
       cmt = fmaxf(cmt, zt_in[j]);
       cms = fmaxf(cms, zs_in[j]);
@@ -77,7 +77,7 @@ __device__ __forceinline__ void fold_chunk(RowStats& r, const float* zt_in, cons
   const float fill = fminf(nmt, nms) - 1024.f / c;  // value of a masked column
   float2 st = make_float2(0.f, 0.f), ss = st, a = st, cc = st;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < W / 2; ++j) {
     float2 zt = make_float2(zt_in[2 * j], zt_in[2 * j + 1]);
     float2 zs = make_float2(zs_in[2 * j], zs_in[2 * j + 1]);
     if (MASKED) {
