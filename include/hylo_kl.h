@@ -33,6 +33,9 @@
  *   - `workspace` is device scratch of at least hylo_kl_workspace_bytes(...) bytes, 256-byte
  *     aligned, not shared with a call still running on another stream.
  *   - Calls require an sm_103 device (GB300); otherwise HYLO_ERR_ARCH. There is no fallback.
+ *   - Calls may be captured into a CUDA graph once one call has run eagerly on the device (it
+ *     sets the kernels up). Replays give the same results; a replayed forward reuses its
+ *     captured pacing tag, so it runs without cluster pacing (a little more DRAM traffic).
  *
  * Accuracy (against an fp64 evaluation of the formulas above, bf16 inputs taken as exact):
  *   - kl[n] within 1e-3 (1 + kl[n]); loss within 1e-4 relative; lse_s, lse_t, lse_gap within
