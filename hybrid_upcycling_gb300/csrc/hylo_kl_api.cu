@@ -130,9 +130,10 @@ hylo_status make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, u
 // their words carry the epoch of the launch that wrote them.
 unsigned next_epoch(DeviceState* d) {
   std::lock_guard<std::mutex> lock(g_mu);
-  d->pace_epoch = d->pace_epoch % 65535u + 1u;
+  d->pace_epoch = d->pace_epoch % 65534u + 2u;  // 2..65535; tag 1 is reserved for captured launches
   return d->pace_epoch;
 }
+
 
 // 3-D tensor map [outer2][outer1][inner] (contiguous), zero fill outside; 128-byte swizzle
 // unless `swizzle` says otherwise.
@@ -191,6 +192,25 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // The fused kernels' pacing counters (one per cluster, then the switch that turns pacing off)
 // follow the statistics or G region.
 constexpr size_t kProgressBytes = ((kMaxClusters + 1) * sizeof(unsigned long long) + 255) & ~size_t(255);
+
+// The pacing words' tag for a forward launch. An eager launch takes the next rolling tag and
+// needs no clearing (words of earlier launches carry other tags). A launch captured into a CUDA
+// graph would replay its captured tag, so during capture the words are cleared on the stream
+// first (the memset is captured with the launch) and the fixed tag 1 is used: every replay
+// starts from cleared words and paces its clusters like an eager launch.
+hylo_status pace_tag(DeviceState* dev, unsigned long long* progress, cudaStream_t stream, unsigned* tag) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cs == cudaStreamCaptureStatusActive) {
+    if ((e = cudaMemsetAsync(progress, 0, kProgressBytes, stream)) != cudaSuccess)
+      return cuda_fail(e, "clear the pacing words");
+    *tag = 1u;
+    return HYLO_OK;
+  }
+  *tag = next_epoch(dev);
+  return HYLO_OK;
+}
 
 // Pacing matters only when clusters run several units each (units > grid); the counters' words
 // hold the unit index in 24 bits.
@@ -297,7 +317,9 @@ hylo_status hylo_kl_forward(const uint16_t* h_s, const uint16_t* W_s, const uint
 
   if (pace_launch(p.units, grid)) {
     p.progress = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + stats_bytes);
-    p.epoch = next_epoch(dev);
+    unsigned tag = 0;
+    if ((st = pace_tag(dev, p.progress, stream, &tag)) != HYLO_OK) return st;
+    p.epoch = tag;
   }
   cudaError_t e = launch_fused(fused_bn(), m_hs, m_Ws, m_ht, m_Wt, p, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "launch fused forward");
@@ -600,10 +622,12 @@ extern "C" hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16
   p.part = scratch;  // every (segment, token) slot read by the combine step is written first
   p.ctl = WaitCtl{dev->status, wait_limit_ns()};
   const int grid = p.units < dev->fused_clusters ? p.units : dev->fused_clusters;
-  if (pace_launch(p.units, grid)) {  // counters at the scratch's tail; epoch-tagged, never cleared
+  if (pace_launch(p.units, grid)) {  // counters at the scratch's tail; epoch-tagged (cleared only under capture)
     p.progress = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(scratch) + kNoAllocScratchBytes -
                                                        kProgressBytes);
-    p.epoch = next_epoch(dev);
+    unsigned tag = 0;
+    if ((st = pace_tag(dev, p.progress, stream, &tag)) != HYLO_OK) return st;
+    p.epoch = tag;
   }
 
   cudaError_t e = launch_fused(fused_bn(), m_hs, m_Ws, m_ht, m_Wt, p, grid, stream);

@@ -34,8 +34,8 @@
  *     aligned, not shared with a call still running on another stream.
  *   - Calls require an sm_103 device (GB300); otherwise HYLO_ERR_ARCH. There is no fallback.
  *   - Calls may be captured into a CUDA graph once one call has run eagerly on the device (it
- *     sets the kernels up). Replays give the same results; a replayed forward reuses its
- *     captured pacing tag, so it runs without cluster pacing (a little more DRAM traffic).
+ *     sets the kernels up). Replays give the same results and pace like eager calls: a forward
+ *     captured with pacing also captures a memset of its 1280 pacing bytes.
  *
  * Accuracy (against an fp64 evaluation of the formulas above, bf16 inputs taken as exact):
  *   - kl[n] within 1e-3 (1 + kl[n]); loss within 1e-4 relative; lse_s, lse_t, lse_gap within
@@ -155,7 +155,7 @@ hylo_status hylo_kl_backward_split(const uint16_t* h_s, const uint16_t* W_s,
  *     current); make that first call before any stream capture.
  *   - All calls share the one array per device and it keeps the last call's contents (each call
  *     writes every statistics slot it reads, and the pacing counters carry the launch's tag,
- *     so nothing needs clearing). Calls that overlap on the GPU
+ *     so nothing needs clearing, except under stream capture, where they are cleared). Calls that overlap on the GPU
  *     (different streams, or threads without ordering) race on it: serialise them. */
 hylo_status hylo_kl_forward_noalloc(const uint16_t* h_s, const uint16_t* W_s,
                                     const uint16_t* h_t, const uint16_t* W_t,

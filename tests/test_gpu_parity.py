@@ -582,11 +582,11 @@ def test_student_wider_than_teacher(d_s, d_t):
 
 def test_forward_and_backward_replay_in_a_cuda_graph():
     """Forward + backward captured into a CUDA graph (after one eager call that sets the library
-    up) and replayed twice: the outputs are bit-identical to the eager calls. Under replay every
-    forward carries the captured pacing epoch, so words left by the previous replay read as
-    finished peers and pacing is simply off; the backward's counters are cleared by the captured
-    memset."""
-    x = gen(2048, 256, 512, 20000, seed=123, w_std=0.08)
+    up) and replayed twice: the outputs are bit-identical to the eager calls. The captured
+    forward clears its pacing words with a captured memset and uses a tag reserved for captured
+    launches, so every replay paces like an eager call; the backward's counters are cleared by
+    its own captured memset."""
+    x = gen(8192, 256, 512, 30000, seed=123, w_std=0.08)  # 224 work units: several waves, paced
     ref = run(x, 1.0)
     N, d_s = x["h_s"].shape
     V, d_t = x["W_t"].shape
@@ -618,3 +618,21 @@ def test_forward_and_backward_replay_in_a_cuda_graph():
         got = dict(kl=kl, lse_s=lse_s, lse_t=lse_t, loss=loss, gap=gap, dh=dh, dW=dW)
         for k in got:
             assert torch.equal(ref[k], got[k]), k
+    # A forward alone, captured and replayed: its pacing words (after the 6 x 32 x N fp32
+    # statistics: one per cluster, at most 128, then the switch; the backward's G ring reuses
+    # that memory, hence the forward-only graph) carry the captured tag 1 and read finished for
+    # every cluster that ran, and pacing was not switched off.
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s):
+        _lib.hylo_kl_forward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], 1.0, 4096, kl, lse_s, lse_t, loss, ws,
+                             stream=s, lse_gap=gap)
+    g2.replay()
+    torch.cuda.synchronize()
+    _lib.hylo_kl_sync_status()
+    assert torch.equal(ref["kl"], kl)
+    off = (6 * 32 * N * 4 + 255) // 256 * 256
+    words = ws[off:off + 8 * 129].view(torch.int64).cpu().tolist()
+    ran = [w for w in words[:128] if (w >> 48) & 0xFFFF == 1]
+    assert len(ran) >= 2
+    assert all(w & ((1 << 48) - 1) == (1 << 48) - 1 for w in ran)
+    assert (words[128] >> 48) & 0xFFFF != 1
