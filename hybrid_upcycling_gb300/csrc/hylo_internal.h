@@ -32,7 +32,7 @@ struct FusedParams {
   float inv_tau;    // 1 / tau
   float* part;      // partial statistics [kStatFields][nseg][N]
   unsigned long long* progress;  // pacing counters [kMaxClusters] + off switch; null: no pacing
-  unsigned epoch;   // 1..65535, different from the previous paced launch on the same counters (1: captured)
+  unsigned epoch;   // 1..65535, different from the previous paced launch on the same counters
   WaitCtl ctl;
 };
 
