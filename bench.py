@@ -665,6 +665,8 @@ def main():
                     help="hidden: the fused hidden-state KL (default); logits: the Fused KL on precomputed logits; "
                          "ild: the Stage-I ILD alignment loss")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured in a CUDA graph (reported as 'graph'; one GPU)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--split-g", action="store_true",
                     help="time hylo_kl_backward_split (G as two bf16 terms) instead of hylo_kl_backward")
@@ -744,6 +746,31 @@ def main():
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     total_ms = max_over_ranks(evs[0][0].elapsed_time(evs[-1][2]), world, dev)
+
+    # ----------------------------------------------------------------- the same step as a CUDA graph
+    graph = None
+    if args.graph and world == 1:
+        # one step (forward + backward: 4 kernels and the backward's counter memset) captured once
+        # and replayed; the per-kernel figures above stay those of the eager loop
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(w, x, b, stream)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ga.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                g.replay()
+        gb.record(stream)
+        torch.cuda.synchronize()
+        _lib.hylo_kl_sync_status(stream)
+        g_ms = ga.elapsed_time(gb)
+        graph = {"ms_per_step": g_ms / args.steps, "value": whole_job_rate(w.N, 1, args.steps, g_ms),
+                 "unit": "tokens/s", "steps": args.steps,
+                 "what": "the step captured once in a CUDA graph and replayed (launch overhead removed)"}
+        del g
     ms_per_step = total_ms / args.steps
     tokens_per_s = whole_job_rate(w.N, world, args.steps, total_ms)
     tflops = w.flops_exec() * world * args.steps / (total_ms / 1e3) / 1e12
@@ -821,6 +848,7 @@ def main():
                          "traffic": traffic, "peak_kind": f"bf16_tflops_sustained ({peak_src})",
                          "flops_per_launch": dom["flops_per_launch"]},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step(w, args.split_g) * args.steps,
+            **({"graph": graph} if graph is not None else {}),
             "clocks": clk.summary(),
             "memory": {"workspace_bytes": int(b["ws"].numel()), "dense_fp32_logits_bytes": 4 * w.N * w.V,
                        "note": "the library allocates nothing; the caller's workspace is its only scratch"},
