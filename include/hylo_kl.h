@@ -84,8 +84,8 @@ size_t hylo_kl_workspace_bytes(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
                                int64_t token_chunk);
 
 /* Forward: kl[N], lse_s[N], lse_t[N] (natural-log units of z/tau) and loss[0] = mean(kl).
- * One fused pass: each CTA computes student and teacher logit tiles on the tensor cores and
- * folds them into running softmax/KL statistics; nothing of size N x V is written.
+ * One fused pass: each CTA pair computes student and teacher logit tiles on the tensor cores
+ * and folds them into running softmax/KL statistics; nothing of size N x V is written.
  * lse_gap[N] is optional (NULL: not written): lse_s - lse_t computed from the statistics as
  * log1p of a sum of per-word differences, so it keeps the digits that the difference of the
  * two fp32 lse values (each rounded at ~1e-6 of log V) loses when the distributions are
@@ -120,13 +120,13 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s,
                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Backward with G kept to ~16 significant bits: G is stored as the sum of two bf16 terms,
- * bf16(G) and bf16(G - bf16(G)), and each token chunk runs the gradient GEMMs twice (the
- * second pass adds the low-order term's products). Same arguments and results as
+ * bf16(G) and bf16(G - bf16(G)), and every dh_s / dW_s tile accumulates the products of both
+ * terms (twice the k-blocks of the plain backward). Same arguments and results as
  * hylo_kl_backward, with a gradient error of ~1e-5 relative instead of the ~1e-3 that one
  * bf16 rounding of G leaves -- which matters where a token's gradient is dominated by one or
  * two words (near one-hot distributions, or a student that differs from its teacher on few
- * words), where one rounding alone can exceed 2e-3. The gradient products run over both
- * terms (twice their k-blocks), and the G ring is doubled (2 x 128 MiB at most): pass at least
+ * words), where one rounding alone can exceed 2e-3. The G ring is doubled (2 x 128 MiB at
+ * most): pass at least
  * hylo_kl_workspace_bytes_split(...) bytes. (The pages describe no such variant; it is a
  * precision option of this library.) */
 size_t hylo_kl_workspace_bytes_split(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
