@@ -126,9 +126,8 @@ hylo_status hylo_kl_backward(const uint16_t* h_s, const uint16_t* W_s,
  * bf16 rounding of G leaves -- which matters where a token's gradient is dominated by one or
  * two words (near one-hot distributions, or a student that differs from its teacher on few
  * words), where one rounding alone can exceed 2e-3. The G ring is doubled (2 x 128 MiB at
- * most): pass at least
- * hylo_kl_workspace_bytes_split(...) bytes. (The pages describe no such variant; it is a
- * precision option of this library.) */
+ * most): pass at least hylo_kl_workspace_bytes_split(...) bytes. (The pages describe no such
+ * variant; it is a precision option of this library.) */
 size_t hylo_kl_workspace_bytes_split(int64_t N, int64_t d_s, int64_t d_t, int64_t V,
                                      int64_t token_chunk);
 hylo_status hylo_kl_backward_split(const uint16_t* h_s, const uint16_t* W_s,
