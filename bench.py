@@ -660,6 +660,8 @@ def main():
                          "take about a millisecond, so that the clock sampler sees the timed region)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="stage2_64k", choices=list(syn.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count N (same shapes otherwise)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="hidden", choices=["hidden", "logits", "ild"],
                     help="hidden: the fused hidden-state KL (default); logits: the Fused KL on precomputed logits; "
@@ -682,6 +684,11 @@ def main():
         args.steps = 10 if args.impl == "reference" else {"hidden": 10, "logits": 300, "ild": 500}[args.path]
     rank, world, local = dist_env()
     w = syn.WORKLOADS[args.workload]
+    if args.tokens is not None:
+        if args.tokens < 1:
+            raise SystemExit("--tokens must be >= 1")
+        # renamed: no DRAM-traffic record (taken per named workload) applies to another N
+        w = w.with_sizes(N=args.tokens, name=f"{w.name}_n{args.tokens}")
 
     if args.impl == "reference":
         run_reference(args, w, rank, world)
