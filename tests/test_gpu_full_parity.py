@@ -138,3 +138,47 @@ def test_full_backward_sampled_rows(full_case):
         assert e_dW <= TOL_GRAD
         del dh, dW, ws
         torch.cuda.empty_cache()
+
+
+def test_64k_launch_configuration_against_the_oracle():
+    """The 64K-token Stage-II workload's shapes and launch configuration as bench.py times it
+    (8 vocabulary segments over paced waves in the forward; 16 token blocks x 24 vocabulary
+    blocks in the backward), with the workload's LM heads and its first U = 1024 token rows
+    repeated over all 65536 positions, so that the fp64 oracle evaluates only the U distinct
+    rows: every token's KL and the exact mean loss, the FULL dW_s (all 128256 rows:
+    sum_u mult(u) G_u^T h_u, G with the global N) and 512 dh_s rows, at the stated tolerances."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    _lib.load()
+    w = syn.WORKLOADS["stage2_64k"]
+    x = syn.make_inputs(w, device="cuda")
+    U, N = 1024, w.N
+    for k in ("h_s", "h_t"):
+        x[k] = x[k][:U].repeat(N // U, 1).contiguous()
+    hu, Ws, htu, Wt = (f64(x[k][:U]) if k.startswith("h") else f64(x[k]) for k in ("h_s", "W_s", "h_t", "W_t"))
+    t0 = time.time()
+    kl_u, _, _, _ = orc.kl_forward(hu, Ws, htu, Wt, w.tau, token_chunk=256)
+    G_u = orc.kl_grad_logits(hu, Ws, htu, Wt, w.tau, 1.0, N)
+    mult = float(N // U)
+    dW_ref = (G_u.T @ hu) * mult
+    loss_ref = float(np.mean(kl_u))
+    print(f"\noracle on {U} distinct rows in {time.time() - t0:.0f} s")
+    g = gpu_forward(w, x)
+    kl_g = f64(g["kl"])
+    kl_ref = np.tile(kl_u, N // U)
+    e_kl = np.max(np.abs(kl_g - kl_ref) / (1 + kl_ref))
+    e_loss = abs(g["loss"].item() - loss_ref) / loss_ref
+    ws = torch.empty(_lib.hylo_kl_workspace_bytes(N, w.d_s, w.d_t, w.V, 4096), dtype=torch.uint8, device="cuda")
+    dh = torch.full((N, w.d_s), float("nan"), device="cuda")
+    dW = torch.full((w.V, w.d_s), float("nan"), device="cuda")
+    _lib.hylo_kl_backward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, 4096, g["lse_s"], g["lse_t"], 1.0, dh, dW,
+                          ws, lse_gap=g["gap"])
+    _lib.hylo_kl_sync_status()
+    e_dW = float(np.linalg.norm(f64(dW) - dW_ref) / np.linalg.norm(dW_ref))
+    rows = token_rows(N, 512, 17)
+    e_dh = float(np.linalg.norm(f64(dh[torch.from_numpy(rows).cuda()]) - G_u[rows % U] @ Ws)
+                 / np.linalg.norm(G_u[rows % U] @ Ws))
+    print(f"64K launch configuration: kl {e_kl:.2e}, mean loss {e_loss:.2e}, dW_s (all rows) {e_dW:.2e}, "
+          f"dh_s 512 rows {e_dh:.2e}")
+    assert e_kl <= TOL_KL and e_loss <= TOL_LOSS and e_dW <= TOL_GRAD and e_dh <= TOL_GRAD
