@@ -140,18 +140,20 @@ def test_full_backward_sampled_rows(full_case):
         torch.cuda.empty_cache()
 
 
-def test_64k_launch_configuration_against_the_oracle():
-    """The 64K-token Stage-II workload's shapes and launch configuration as bench.py times it
-    (8 vocabulary segments over paced waves in the forward; 16 token blocks x 24 vocabulary
-    blocks in the backward), with the workload's LM heads and its first U = 1024 token rows
-    repeated over all 65536 positions, so that the fp64 oracle evaluates only the U distinct
-    rows: every token's KL and the exact mean loss, the FULL dW_s (all 128256 rows:
+@pytest.mark.parametrize("name", ["stage2_64k", "llama3b_nearconv"])
+def test_64k_launch_configuration_against_the_oracle(name):
+    """A 64K-token workload's shapes and launch configuration as bench.py times it (vocabulary
+    segments over paced waves in the forward; 16 token blocks x 24 vocabulary blocks in the
+    backward), with the workload's LM heads and its first U = 1024 token rows repeated over all
+    65536 positions, so that the fp64 oracle evaluates only the U distinct rows: every token's
+    KL and the exact mean loss (for the near-converged workload, KL ~ 7e-5 per token: the 1e-4
+    relative mean-loss bound at full size), the FULL dW_s (all 128256 rows:
     sum_u mult(u) G_u^T h_u, G with the global N) and 512 dh_s rows, at the stated tolerances."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     build.build()
     _lib.load()
-    w = syn.WORKLOADS["stage2_64k"]
+    w = syn.WORKLOADS[name]
     x = syn.make_inputs(w, device="cuda")
     U, N = 1024, w.N
     for k in ("h_s", "h_t"):
@@ -179,6 +181,6 @@ def test_64k_launch_configuration_against_the_oracle():
     rows = token_rows(N, 512, 17)
     e_dh = float(np.linalg.norm(f64(dh[torch.from_numpy(rows).cuda()]) - G_u[rows % U] @ Ws)
                  / np.linalg.norm(G_u[rows % U] @ Ws))
-    print(f"64K launch configuration: kl {e_kl:.2e}, mean loss {e_loss:.2e}, dW_s (all rows) {e_dW:.2e}, "
+    print(f"{name} launch configuration: kl {e_kl:.2e}, mean loss {e_loss:.2e}, dW_s (all rows) {e_dW:.2e}, "
           f"dh_s 512 rows {e_dh:.2e}")
     assert e_kl <= TOL_KL and e_loss <= TOL_LOSS and e_dW <= TOL_GRAD and e_dh <= TOL_GRAD
