@@ -184,3 +184,18 @@ def test_64k_launch_configuration_against_the_oracle(name):
     print(f"{name} launch configuration: kl {e_kl:.2e}, mean loss {e_loss:.2e}, dW_s (all rows) {e_dW:.2e}, "
           f"dh_s 512 rows {e_dh:.2e}")
     assert e_kl <= TOL_KL and e_loss <= TOL_LOSS and e_dW <= TOL_GRAD and e_dh <= TOL_GRAD
+    if name != "stage2_64k":
+        return
+    # the precise backward (G as two bf16 terms) at the same configuration: dW_s to 1e-4; dh_s to
+    # the bound of its fp32 accumulation over K = V in steps of 16, (V / 16) 2^-24
+    del ws
+    ws2 = torch.empty(_lib.hylo_kl_workspace_bytes_split(N, w.d_s, w.d_t, w.V, 4096), dtype=torch.uint8,
+                      device="cuda")
+    _lib.hylo_kl_backward_split(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, 4096, g["lse_s"], g["lse_t"], 1.0,
+                                dh, dW, ws2, lse_gap=g["gap"])
+    _lib.hylo_kl_sync_status()
+    s_dW = float(np.linalg.norm(f64(dW) - dW_ref) / np.linalg.norm(dW_ref))
+    s_dh = float(np.linalg.norm(f64(dh[torch.from_numpy(rows).cuda()]) - G_u[rows % U] @ Ws)
+                 / np.linalg.norm(G_u[rows % U] @ Ws))
+    print(f"{name} split backward: dW_s (all rows) {s_dW:.2e}, dh_s 512 rows {s_dh:.2e}")
+    assert s_dW <= 1e-4 and s_dh <= (w.V / 16) * 2.0 ** -24
