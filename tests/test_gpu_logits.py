@@ -190,3 +190,27 @@ def test_autograd_wrapper_matches_oracle():
     (2.5 * loss).backward()
     assert np.linalg.norm(f64(zs.grad) - 2.5 * G) / np.linalg.norm(2.5 * G) <= 2 * TOL_GRAD
     assert z_t.grad is None
+
+
+def test_bench_configuration_against_the_oracle():
+    """65536 x 128256 logits, the size bench.py --path logits times, with the workload's first
+    U = 1024 rows repeated over all rows, so that the fp64 oracle evaluates only U distinct rows:
+    every row's KL and the exact mean loss, dz_s on 512 rows spread over the range, and rows with
+    equal inputs give equal bits."""
+    w = syn.WORKLOADS["stage2_64k"]
+    z = syn.make_logits(w.with_sizes(N=1024), device="cuda")
+    U, N = 1024, w.N
+    z_s = z["z_s"].repeat(N // U, 1).contiguous()
+    z_t = z["z_t"].repeat(N // U, 1).contiguous()
+    kl_u, _, _, loss_u, G_u = orc.kl_from_logits(f64(z["z_s"]), f64(z["z_t"]), w.tau)
+    G_u *= U / N  # the oracle normalised by its own U rows; the kernel by all N
+    g = run(z_s, z_t, w.tau)
+    kl_ref = np.tile(kl_u, N // U)
+    assert np.all(np.abs(f64(g["kl"]) - kl_ref) <= TOL_KL * (1 + kl_ref))
+    assert abs(g["loss"].item() - loss_u) <= TOL_LOSS * loss_u
+    rows = np.array(sorted({0, 1, U - 1, U, N - 1} | set(np.random.default_rng(3).choice(N, 507, replace=False).tolist())))
+    r = torch.from_numpy(rows).cuda()
+    err = np.linalg.norm(f64(g["dz"][r]) - G_u[rows % U]) / np.linalg.norm(G_u[rows % U])
+    print(f"logits 65536 x 128256: dz rows rel {err:.2e}")
+    assert err <= TOL_GRAD
+    assert torch.equal(g["dz"][r], g["dz"][torch.from_numpy(rows % U).cuda()])
