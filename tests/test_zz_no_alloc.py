@@ -55,3 +55,38 @@ def test_noalloc_forward_matches_workspace_forward():
         assert abs(loss[0] - r_loss[0]) <= TOL_LOSS * abs(r_loss[0]), call
         assert np.all(np.abs(ls - r_ls) <= TOL_LSE * (1 + np.abs(r_ls))), call
         assert np.all(np.abs(lt - r_lt) <= TOL_LSE * (1 + np.abs(r_lt))), call
+
+
+@pytest.mark.gpu
+def test_noalloc_forward_at_its_token_limit():
+    """N = 698997, the largest N the built-in array holds: the statistics fill it to its last
+    statistics byte (fewer vocabulary segments than the workspace forward would use, so the
+    results agree with it to fp32 summation order) and the launch paces its clusters with the
+    counters at the array's tail. Checked against the workspace forward and, on 300 sampled
+    rows including the last, against the fp64 oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    from oracle import kl_oracle as orc
+    w = syn.Workload("limit", 0, 698997, 64, 64, 2000, 1.0, 0.1, False)
+    x = syn.make_inputs(w, device="cuda", seed=5)
+    N = w.N
+    f = dict(dtype=torch.float32, device="cuda")
+    ws = torch.empty(_lib.hylo_kl_workspace_bytes(N, w.d_s, w.d_t, w.V, 4096), dtype=torch.uint8, device="cuda")
+    ref = [torch.empty(N, **f), torch.empty(N, **f), torch.empty(N, **f), torch.empty(1, **f)]
+    _lib.hylo_kl_forward(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, 4096, *ref, ws)
+    out = [torch.full((N,), float("nan"), **f) for _ in range(3)] + [torch.full((1,), float("nan"), **f)]
+    _lib.hylo_kl_forward_noalloc(x["h_s"], x["W_s"], x["h_t"], x["W_t"], w.tau, 4096, *out)
+    _lib.hylo_kl_sync_status()
+    kl, ls, lt, loss = (t.double().cpu().numpy() for t in out)
+    r_kl, r_loss = ref[0].double().cpu().numpy(), ref[3].item()
+    assert np.all(np.isfinite(kl))
+    assert np.all(np.abs(kl - r_kl) <= TOL_KL * (1 + r_kl))
+    assert abs(loss[0] - r_loss) <= TOL_LOSS * abs(r_loss)
+    rows = np.array(sorted({0, N - 1, N - 2} | set(np.random.default_rng(1).choice(N, 297, replace=False).tolist())))
+    a = {k: x[k].double().cpu().numpy() for k in ("W_s", "W_t")}
+    hs, ht = x["h_s"][torch.from_numpy(rows).cuda()].double().cpu().numpy(), x["h_t"][torch.from_numpy(rows).cuda()].double().cpu().numpy()
+    o_kl, o_ls, o_lt, _ = orc.kl_rows(hs, a["W_s"], ht, a["W_t"], w.tau, np.arange(len(rows)))
+    assert np.all(np.abs(kl[rows] - o_kl) <= TOL_KL * (1 + o_kl))
+    assert np.all(np.abs(ls[rows] - o_ls) <= TOL_LSE * (1 + np.abs(o_ls)))
+    assert np.all(np.abs(lt[rows] - o_lt) <= TOL_LSE * (1 + np.abs(o_lt)))
